@@ -1,0 +1,260 @@
+/*
+ * locks.h - C ABI of the LOCKS decode-step library for GB300 (sm_103a).
+ *
+ * LOCKS ("page-local compact key summaries") keeps, for every 16-token page
+ * of a paged bf16 K/V cache and every kv head, a small resident summary of
+ * the page's keys, and at each decode step reads only those summaries to
+ * choose the pages that receive full attention. Source pages:
+ *   [post]    "LOCKS: per-page SVD cuts KV cache reads 10x at 1M context"
+ *             (wps.hkprog.org), sections "How LOCKS works" and "Code".
+ *   [summary] gist.science technical summary of arXiv 2607.24555, section 2
+ *             "Method" (2.1 page-local spectral decomposition, 2.2
+ *             reconstruction and selection, 2.3 group-shared selection,
+ *             2.4 implementation).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named *_cache, q, scores, selected, out, lse, workspace and the
+ *   summary arrays are DEVICE pointers (16-byte aligned; scales 8-byte).
+ *   dims is a HOST pointer. The caller owns every buffer; the library
+ *   allocates nothing and keeps no state besides cached device attributes.
+ * - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Every call is asynchronous on that stream, performs no host
+ *   synchronisation and no allocation, and so may be captured in a CUDA graph.
+ * - Return value: LOCKS_OK, or a negative LOCKS_ERR_* code. Argument errors
+ *   are detected on the host before anything is launched. LOCKS_ERR_CUDA means
+ *   a launch failed (cudaGetLastError was not cudaSuccess). Errors that can
+ *   only be seen on the device (a bounded wait that ran out) are recorded in
+ *   the device status word at the start of the workspace; read it with
+ *   locks_get_device_status. The standalone calls accept workspace = NULL
+ *   (then device-side errors are not recorded); locks_decode_step needs
+ *   locks_workspace_size bytes. Page ids read on the device are range-checked
+ *   (LOCKS_ERR_BAD_INDEX) so a bad table cannot make a kernel read outside
+ *   the caller's buffers.
+ * - Fixed sizes: head_dim 128, page_size 16, rank 8. num_kv_heads must be 1,
+ *   2, 4 or 8 and num_q_heads / num_kv_heads (the GQA group g) at most 16.
+ *   Other values return LOCKS_ERR_UNSUPPORTED.
+ * - Query head h attends through kv head h / g.
+ *
+ * Memory layouts
+ * --------------
+ *   k_cache, v_cache  bf16 bits [num_phys_pages][num_kv_heads][16][128]
+ *   q                 fp32 [batch][num_q_heads][128]
+ *   page_table        int32 [batch][max_pages_per_seq]: logical -> physical page
+ *   seq_pages         int32 [batch]: full (summarised) pages of each sequence,
+ *                     0 <= seq_pages[b] <= max_pages_per_seq
+ *   scores            fp32 [batch][num_q_heads][max_pages_per_seq]
+ *   selected          int32 [batch][num_kv_heads][k_cap], ascending logical
+ *                     page ids, k_cap = locks_k_cap(dims, budget_tokens)
+ *   n_selected        int32 [batch][num_kv_heads]
+ *   out               bf16 bits [batch][num_q_heads][128]
+ *   lse               fp32 [batch][num_q_heads] (natural log), may be NULL
+ *
+ * Summary layout (one "unit" = one (physical page, kv head); 776 bytes)
+ *   mu     int8  [num_phys_pages][num_kv_heads][128]
+ *   basis  uint8 [num_phys_pages][num_kv_heads][512]  (int4 codes)
+ *   coef   int8  [num_phys_pages][num_kv_heads][128]
+ *   scales fp16 bits [num_phys_pages][num_kv_heads][4] = absmax scales of
+ *          mu, basis, coef, then 0
+ * Value = code * scale. Codes are symmetric: int8 in [-127, 127], int4 (two's
+ * complement nibble) in [-7, 7]. Inside a unit, elements sit in the order the
+ * scoring kernel's tensor-core fragments read them:
+ *   mu[d]       at byte 32*t + 4*s + 2*h + e
+ *   basis[d][r] in byte 64*r + 16*t + 4*(s/2) + p/2, nibble p%2 (0 = low 4 bits),
+ *               p = 2*(s%2) + h + 4*e
+ *   coef[i][r]  at byte 4*(4*(i%8) + r/2) + 2*(i/8) + r%2
+ * where for a head dimension d: s = d/16, w = d%16, h = w/8, t = (w%8)/2,
+ * e = w%2; i is the token (0..15) and r the rank (0..7).
+ */
+#ifndef LOCKS_H
+#define LOCKS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(LOCKS_BUILD) && defined(__GNUC__)
+#define LOCKS_API __attribute__((visibility("default")))
+#else
+#define LOCKS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LOCKS_HEAD_DIM 128
+#define LOCKS_PAGE_SIZE 16
+#define LOCKS_RANK 8
+#define LOCKS_MAX_GROUP 16
+#define LOCKS_UNIT_BYTES 776
+
+enum {
+    LOCKS_OK = 0,
+    LOCKS_ERR_INVALID_ARG = -1,        /* null pointer, negative or inconsistent size */
+    LOCKS_ERR_UNSUPPORTED = -2,        /* head_dim/page/rank/heads outside what is built */
+    LOCKS_ERR_WORKSPACE_TOO_SMALL = -3,
+    LOCKS_ERR_CUDA = -4,               /* a CUDA runtime call or launch failed */
+    LOCKS_ERR_TIMEOUT = -5,            /* device: a bounded wait ran out (status word) */
+    LOCKS_ERR_BAD_INDEX = -6,          /* device: a page id or page-table entry out of range;
+                                          the unit was skipped or read from page 0 instead */
+};
+
+typedef struct {
+    int32_t batch;              /* B: sequences (requests) */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv; g = Hq / Hkv */
+    int32_t head_dim;           /* must be 128 */
+    int32_t page_size;          /* must be 16 */
+    int32_t rank;               /* must be 8 */
+    int32_t max_pages_per_seq;  /* row stride of page_table and scores */
+    int32_t num_phys_pages;     /* pages in the K/V pool and in the summary arrays */
+} locks_dims_t;
+
+typedef struct {
+    int8_t* mu;         /* [num_phys_pages][Hkv][128]  device */
+    uint8_t* basis;     /* [num_phys_pages][Hkv][512]  device */
+    int8_t* coef;       /* [num_phys_pages][Hkv][128]  device */
+    uint16_t* scales;   /* [num_phys_pages][Hkv][4]    device, fp16 bits */
+} locks_summaries_t;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+LOCKS_API int locks_version(void);
+
+/* Human-readable name of a status code. Never NULL. */
+LOCKS_API const char* locks_status_string(int status);
+
+/*
+ * k_cap: row stride of `selected` = min(budget_tokens / 16, max_pages_per_seq),
+ * at least 1. The number of pages kept per (sequence, kv head) is
+ * k = min(budget_tokens / 16, seq_pages[b])  ([post] "Code": budget // page).
+ * Returns LOCKS_ERR_INVALID_ARG for a null dims or a negative budget.
+ */
+LOCKS_API int locks_k_cap(const locks_dims_t* dims, int32_t budget_tokens, int32_t* k_cap);
+
+/*
+ * Workspace bytes needed by every call below for these dims and budget
+ * (the decode step needs the most: the score table, the selection and the
+ * device status word). The workspace must be 256-byte aligned. Its first 256
+ * bytes hold the status word; locks_clear_device_status zeroes it.
+ */
+LOCKS_API int locks_workspace_size(const locks_dims_t* dims, int32_t budget_tokens, size_t* bytes);
+
+/*
+ * Summary build ([post] "How LOCKS works": a one-time decomposition of the
+ * centred keys when a page fills, off the decode critical path; [summary] 2.1:
+ * a small eigendecomposition of the centred keys, int8 centroid, int4 basis,
+ * int8 coefficients, about 10% of the page's K/V bytes).
+ * For each listed physical page p = phys_page_ids[i] (0 <= i < n_pages) and
+ * each kv head: mu = mean of the 16 keys; D = K - mu; eigenpairs of the 16x16
+ * Gram D D^T (descending); for the top 8: V[:, r] = D^T u_r / sqrt(lambda_r),
+ * C[:, r] = sqrt(lambda_r) u_r, a column with lambda_r <= 1e-12 lambda_1 is
+ * zero; the largest-magnitude entry of each V column is made positive; then
+ * absmax-quantised into the summary layout above. Pages not listed are left
+ * untouched. Computed in fp32 on the GPU.
+ */
+LOCKS_API int locks_build_summaries(const locks_dims_t* dims, const uint16_t* k_cache,
+                                    const int32_t* phys_page_ids, int32_t n_pages,
+                                    locks_summaries_t summaries, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
+ * Page scores from the summaries alone ([post] "How LOCKS works" and
+ * [summary] 2.2; no key or value is read):
+ *   scores[b][h][j] = log sum_{i < 16} exp[(q.mu_j + (V_j^T q).c_i) / sqrt(128)]
+ * for every sequence b, query head h and logical page j < seq_pages[b], with
+ * the summary of unit (page_table[b][j], h / g) dequantised. Entries
+ * j >= seq_pages[b] are not written.
+ */
+LOCKS_API int locks_score_pages(const locks_dims_t* dims, const float* q, locks_summaries_t summaries,
+                                const int32_t* page_table, const int32_t* seq_pages, float* scores,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Group-shared top-k selection ([summary] 2.3: mean of the estimated mass
+ * shares over the query heads of a GQA group; [post] "Code": keep
+ * budget // 16 pages, indices sorted ascending).
+ *   L_h   = log sum_{j < seq_pages[b]} exp(scores[b][h][j])
+ *   key_j = log( (1/g) sum_{h in group} exp(scores[b][h][j] - L_h) )
+ * selected[b][kvh][0..k) = the k logical pages with the largest key (radix
+ * select on the order-preserving 32-bit image of key), equal keys ranked by
+ * lower page id, NaN keys ranked below -inf, written in ascending order;
+ * n_selected[b][kvh] = k. sel_keys (fp32 [B][Hkv][max_pages_per_seq], may be
+ * NULL) receives key_j for j < seq_pages[b].
+ */
+LOCKS_API int locks_select_pages(const locks_dims_t* dims, const float* scores, const int32_t* seq_pages,
+                                 int32_t budget_tokens, int32_t* selected, int32_t* n_selected,
+                                 float* sel_keys, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Attention over the selected pages only ([post] "Code": scaled dot-product
+ * attention of q over the keys/values of the chosen pages, scale 1/sqrt(128)):
+ *   out[b][h] = sum_t softmax_t(q.k_t / sqrt(128)) v_t,  lse[b][h] = log sum_t exp(.)
+ * over the 16 tokens of each page selected[b][h/g][0..n_selected[b][h/g]),
+ * read through page_table. Split-K across the CTAs of a thread-block cluster
+ * per (b, kv head), merged with the online-softmax rule. k_cap is the row
+ * stride of `selected`. n = 0 gives out = 0 and lse = -inf.
+ */
+LOCKS_API int locks_sparse_attention(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                     const uint16_t* v_cache, const int32_t* page_table,
+                                     const int32_t* selected, const int32_t* n_selected, int32_t k_cap,
+                                     uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * Selection and sparse attention fused in one cluster kernel: exactly
+ * locks_select_pages followed by locks_sparse_attention on its result, in one
+ * launch (the selection never leaves the cluster except through `selected`,
+ * which the kernel writes and re-reads). selected is [B][Hkv][k_cap] with
+ * k_cap = locks_k_cap(dims, budget_tokens); n_selected is [B][Hkv].
+ */
+LOCKS_API int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                  const uint16_t* v_cache, const int32_t* page_table, const float* scores,
+                                  const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected,
+                                  int32_t* n_selected, uint16_t* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * The whole decode step ([summary] 2.4: scoring, selection and sparse
+ * attention captured together in CUDA graphs): locks_score_pages, then
+ * locks_select_attend.
+ * scores, selected and n_selected may be NULL, in which case they live in the
+ * workspace; when given they receive the same values as the separate calls.
+ * Two kernel launches; no host synchronisation; graph-capturable.
+ */
+LOCKS_API int locks_decode_step(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                const uint16_t* v_cache, locks_summaries_t summaries,
+                                const int32_t* page_table, const int32_t* seq_pages, int32_t budget_tokens,
+                                uint16_t* out, float* lse, float* scores, int32_t* selected,
+                                int32_t* n_selected, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Copies the device status word (LOCKS_OK, LOCKS_ERR_TIMEOUT or
+ * LOCKS_ERR_BAD_INDEX; the first error recorded wins) at the start of the
+ * workspace to *status. Synchronises the stream.
+ */
+LOCKS_API int locks_get_device_status(const void* workspace, int32_t* status, void* stream);
+
+/* Zeroes the device status word (asynchronous on stream). */
+LOCKS_API int locks_clear_device_status(void* workspace, void* stream);
+
+/*
+ * Device-side bounded waits: sets the wall-time limit in nanoseconds that
+ * every later launch from this process gives its mbarrier waits (0 restores
+ * the default of 2 s). Host-side setting, read at launch time.
+ */
+LOCKS_API int locks_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Failure-detection self test (no counterpart on the LOCKS pages): launches
+ * one CTA that waits on an mbarrier phase nothing will complete. The wait
+ * gives up after limit_ns and records LOCKS_ERR_TIMEOUT in the status word of
+ * `workspace` (>= 256 bytes); the context stays usable. Asynchronous.
+ */
+LOCKS_API int locks_selftest_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOCKS_H */

@@ -1,0 +1,399 @@
+// api.cu - the C ABI of include/locks.h: argument validation, workspace
+// layout and kernel launches. No allocation, no host synchronisation (except
+// locks_get_device_status), so every compute call can be captured in a CUDA
+// graph.
+#include <atomic>
+#include <mutex>
+
+#include "locks_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
+constexpr int kMaxDevices = 64;
+
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+int num_sms(int dev) {
+    static std::atomic<int> cache[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    int v = cache[dev].load();
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev].store(v);
+    return v;
+}
+
+// Cluster size for the select/attend kernels, cached per (device, mode, smem).
+int cluster_size(int dev, int max_pages, locks::SAMode mode) {
+    struct Entry {
+        int dev, mode;
+        size_t smem;
+        int cl;
+    };
+    static std::mutex mu;
+    static Entry table[64];
+    static int n = 0;
+    const size_t smem16 = locks::select_attend_smem_bytes(max_pages, 16, mode);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (table[i].dev == dev && table[i].mode == static_cast<int>(mode) && table[i].smem == smem16)
+            return table[i].cl;
+    const int cl = locks::select_attend_cluster_size(max_pages, mode);
+    if (n < 64) table[n++] = {dev, static_cast<int>(mode), smem16, cl};
+    return cl;
+}
+
+locks::DeviceStatus status_of(void* ws) {
+    locks::DeviceStatus st;
+    st.word = reinterpret_cast<int32_t*>(ws);
+    st.wait_limit_ns = g_wait_limit_ns.load();
+    return st;
+}
+
+int validate_dims(const locks_dims_t* d) {
+    if (!d) return LOCKS_ERR_INVALID_ARG;
+    if (d->head_dim != LOCKS_HEAD_DIM || d->page_size != LOCKS_PAGE_SIZE || d->rank != LOCKS_RANK)
+        return LOCKS_ERR_UNSUPPORTED;
+    if (d->batch < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->max_pages_per_seq < 0 ||
+        d->num_phys_pages < 0)
+        return LOCKS_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads != 0) return LOCKS_ERR_INVALID_ARG;
+    const int hkv = d->num_kv_heads;
+    if (hkv != 1 && hkv != 2 && hkv != 4 && hkv != 8) return LOCKS_ERR_UNSUPPORTED;
+    if (d->num_q_heads / hkv > LOCKS_MAX_GROUP) return LOCKS_ERR_UNSUPPORTED;
+    if (d->batch > 0 && d->max_pages_per_seq > 0 && d->num_phys_pages <= 0) return LOCKS_ERR_INVALID_ARG;
+    return LOCKS_OK;
+}
+
+int k_cap_of(const locks_dims_t* d, int32_t budget) {
+    int k = budget / LOCKS_PAGE_SIZE;
+    if (k > d->max_pages_per_seq) k = d->max_pages_per_seq;
+    return k < 1 ? 1 : k;
+}
+
+struct WsLayout {
+    size_t status, scores, selected, n_selected, total;
+};
+WsLayout ws_layout(const locks_dims_t* d, int32_t budget) {
+    WsLayout w;
+    const size_t B = static_cast<size_t>(d->batch);
+    w.status = 0;
+    w.scores = kAlign;
+    w.selected = w.scores + align_up(B * d->num_q_heads * static_cast<size_t>(d->max_pages_per_seq) * 4);
+    w.n_selected = w.selected + align_up(B * d->num_kv_heads * static_cast<size_t>(k_cap_of(d, budget)) * 4);
+    w.total = w.n_selected + align_up(B * d->num_kv_heads * 4);
+    return w;
+}
+
+int check_ws(void* ws, size_t bytes, size_t need) {
+    if (!ws) return need == 0 ? LOCKS_OK : LOCKS_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(ws, kAlign)) return LOCKS_ERR_INVALID_ARG;
+    if (bytes < need) return LOCKS_ERR_WORKSPACE_TOO_SMALL;
+    return LOCKS_OK;
+}
+
+int check_summaries(const locks_summaries_t& s) {
+    if (!s.mu || !s.basis || !s.coef || !s.scales) return LOCKS_ERR_INVALID_ARG;
+    if (!aligned(s.mu, 16) || !aligned(s.basis, 16) || !aligned(s.coef, 16) || !aligned(s.scales, 8))
+        return LOCKS_ERR_INVALID_ARG;
+    return LOCKS_OK;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return LOCKS_OK;
+    cudaGetLastError();
+    return LOCKS_ERR_CUDA;
+}
+
+bool select_fits(int max_pages, locks::SAMode mode) {
+    return locks::select_attend_smem_bytes(max_pages, 8, mode) <= 200 * 1024;
+}
+
+int score_impl(const locks_dims_t* dims, const float* q, locks_summaries_t s, const int32_t* page_table,
+               const int32_t* seq_pages, float* scores, void* ws, cudaStream_t stream) {
+    const int dev = current_device();
+    if (dev < 0) return LOCKS_ERR_CUDA;
+    locks::ScoreArgs a;
+    a.q = q;
+    a.mu = s.mu;
+    a.basis = s.basis;
+    a.coef = s.coef;
+    a.scales = s.scales;
+    a.page_table = page_table;
+    a.seq_pages = seq_pages;
+    a.scores = scores;
+    a.batch = dims->batch;
+    a.hq = dims->num_q_heads;
+    a.hkv = dims->num_kv_heads;
+    a.max_pages = dims->max_pages_per_seq;
+    a.num_phys = dims->num_phys_pages;
+    a.st = status_of(ws);
+    return cuda_status(locks::launch_score(a, num_sms(dev), stream));
+}
+
+locks::SelectAttendArgs sa_args(const locks_dims_t* dims, void* ws) {
+    locks::SelectAttendArgs a = {};
+    a.batch = dims->batch;
+    a.hq = dims->num_q_heads;
+    a.hkv = dims->num_kv_heads;
+    a.max_pages = dims->max_pages_per_seq;
+    a.num_phys = dims->num_phys_pages;
+    a.st = status_of(ws);
+    return a;
+}
+
+int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                       const int32_t* page_table, const float* scores, const int32_t* seq_pages,
+                       int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
+                       void* workspace, cudaStream_t st) {
+    const int dev = current_device();
+    if (dev < 0) return LOCKS_ERR_CUDA;
+    locks::SelectAttendArgs a = sa_args(dims, workspace);
+    a.scores = scores;
+    a.seq_pages = seq_pages;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.sel_keys = nullptr;
+    a.budget_pages = budget_tokens / LOCKS_PAGE_SIZE;
+    a.k_cap = k_cap_of(dims, budget_tokens);
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.page_table = page_table;
+    a.out = out;
+    a.lse = lse;
+    const int cl = cluster_size(dev, dims->max_pages_per_seq, locks::SAMode::kSelectAttend);
+    return cuda_status(locks::launch_select_attend(a, locks::SAMode::kSelectAttend, cl, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int locks_version(void) { return 10000; }
+
+const char* locks_status_string(int status) {
+    switch (status) {
+        case LOCKS_OK: return "ok";
+        case LOCKS_ERR_INVALID_ARG: return "invalid argument";
+        case LOCKS_ERR_UNSUPPORTED: return "unsupported size";
+        case LOCKS_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case LOCKS_ERR_CUDA: return "CUDA launch or runtime error";
+        case LOCKS_ERR_TIMEOUT: return "device wait timed out";
+        case LOCKS_ERR_BAD_INDEX: return "page index out of range on the device";
+        default: return "unknown status";
+    }
+}
+
+int locks_k_cap(const locks_dims_t* dims, int32_t budget_tokens, int32_t* k_cap) {
+    if (!dims || !k_cap || budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
+    *k_cap = k_cap_of(dims, budget_tokens);
+    return LOCKS_OK;
+}
+
+int locks_workspace_size(const locks_dims_t* dims, int32_t budget_tokens, size_t* bytes) {
+    if (!bytes || budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
+    const int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    *bytes = ws_layout(dims, budget_tokens).total;
+    return LOCKS_OK;
+}
+
+int locks_set_wait_limit_ns(uint64_t ns) {
+    g_wait_limit_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+    return LOCKS_OK;
+}
+
+int locks_build_summaries(const locks_dims_t* dims, const uint16_t* k_cache, const int32_t* phys_page_ids,
+                          int32_t n_pages, locks_summaries_t summaries, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    if (n_pages < 0) return LOCKS_ERR_INVALID_ARG;
+    if (n_pages == 0) return LOCKS_OK;
+    if (!k_cache || !phys_page_ids || !aligned(k_cache, 16)) return LOCKS_ERR_INVALID_ARG;
+    if ((v = check_summaries(summaries)) != LOCKS_OK) return v;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    const int dev = current_device();
+    if (dev < 0) return LOCKS_ERR_CUDA;
+    locks::BuildArgs a;
+    a.k_cache = k_cache;
+    a.phys_page_ids = phys_page_ids;
+    a.n_pages = n_pages;
+    a.hkv = dims->num_kv_heads;
+    a.num_phys = dims->num_phys_pages;
+    a.mu = summaries.mu;
+    a.basis = summaries.basis;
+    a.coef = summaries.coef;
+    a.scales = summaries.scales;
+    a.st = status_of(workspace);
+    return cuda_status(locks::launch_build(a, num_sms(dev), static_cast<cudaStream_t>(stream)));
+}
+
+int locks_score_pages(const locks_dims_t* dims, const float* q, locks_summaries_t summaries,
+                      const int32_t* page_table, const int32_t* seq_pages, float* scores, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    if (dims->batch == 0 || dims->max_pages_per_seq == 0) return LOCKS_OK;
+    if (!q || !page_table || !seq_pages || !scores || !aligned(q, 16)) return LOCKS_ERR_INVALID_ARG;
+    if ((v = check_summaries(summaries)) != LOCKS_OK) return v;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    return score_impl(dims, q, summaries, page_table, seq_pages, scores, workspace,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int locks_select_pages(const locks_dims_t* dims, const float* scores, const int32_t* seq_pages,
+                       int32_t budget_tokens, int32_t* selected, int32_t* n_selected, float* sel_keys,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!scores || !seq_pages || !selected || !n_selected) return LOCKS_ERR_INVALID_ARG;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelect)) return LOCKS_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LOCKS_ERR_CUDA;
+    locks::SelectAttendArgs a = sa_args(dims, workspace);
+    a.scores = scores;
+    a.seq_pages = seq_pages;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.sel_keys = sel_keys;
+    a.budget_pages = budget_tokens / LOCKS_PAGE_SIZE;
+    a.k_cap = k_cap_of(dims, budget_tokens);
+    const int cl = cluster_size(dev, dims->max_pages_per_seq, locks::SAMode::kSelect);
+    return cuda_status(locks::launch_select_attend(a, locks::SAMode::kSelect, cl, static_cast<cudaStream_t>(stream)));
+}
+
+int locks_sparse_attention(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                           const uint16_t* v_cache, const int32_t* page_table, const int32_t* selected,
+                           const int32_t* n_selected, int32_t k_cap, uint16_t* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    if (k_cap < 1) return LOCKS_ERR_INVALID_ARG;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !selected || !n_selected || !out) return LOCKS_ERR_INVALID_ARG;
+    if (!aligned(q, 8) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return LOCKS_ERR_INVALID_ARG;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    const int dev = current_device();
+    if (dev < 0) return LOCKS_ERR_CUDA;
+    locks::SelectAttendArgs a = sa_args(dims, workspace);
+    a.selected = const_cast<int32_t*>(selected);
+    a.n_selected = const_cast<int32_t*>(n_selected);
+    a.k_cap = k_cap;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.page_table = page_table;
+    a.out = out;
+    a.lse = lse;
+    const int cl = cluster_size(dev, dims->max_pages_per_seq, locks::SAMode::kAttend);
+    return cuda_status(locks::launch_select_attend(a, locks::SAMode::kAttend, cl, static_cast<cudaStream_t>(stream)));
+}
+
+int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const int32_t* page_table, const float* scores, const int32_t* seq_pages,
+                        int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !scores || !seq_pages || !selected || !n_selected || !out)
+        return LOCKS_ERR_INVALID_ARG;
+    if (!aligned(q, 8) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return LOCKS_ERR_INVALID_ARG;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelectAttend)) return LOCKS_ERR_UNSUPPORTED;
+    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
+                              n_selected, out, lse, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int locks_decode_step(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                      locks_summaries_t summaries, const int32_t* page_table, const int32_t* seq_pages,
+                      int32_t budget_tokens, uint16_t* out, float* lse, float* scores, int32_t* selected,
+                      int32_t* n_selected, void* workspace, size_t workspace_bytes, void* stream) {
+    int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(dims, budget_tokens);
+    if ((v = check_ws(workspace, workspace_bytes, L.total)) != LOCKS_OK) return v;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_pages || !out) return LOCKS_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return LOCKS_ERR_INVALID_ARG;
+    if ((v = check_summaries(summaries)) != LOCKS_OK) return v;
+    if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelectAttend)) return LOCKS_ERR_UNSUPPORTED;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    if (!scores) scores = reinterpret_cast<float*>(base + L.scores);
+    if (!selected) selected = reinterpret_cast<int32_t*>(base + L.selected);
+    if (!n_selected) n_selected = reinterpret_cast<int32_t*>(base + L.n_selected);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->max_pages_per_seq > 0) {
+        v = score_impl(dims, q, summaries, page_table, seq_pages, scores, workspace, st);
+        if (v != LOCKS_OK) return v;
+    }
+    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
+                              n_selected, out, lse, workspace, st);
+}
+
+int locks_get_device_status(const void* workspace, int32_t* status, void* stream) {
+    if (!workspace || !status) return LOCKS_ERR_INVALID_ARG;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    *status = host;
+    return LOCKS_OK;
+}
+
+int locks_clear_device_status(void* workspace, void* stream) {
+    if (!workspace) return LOCKS_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+}
+
+int locks_selftest_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t limit_ns, void* stream) {
+    if (!workspace) return LOCKS_ERR_INVALID_ARG;
+    const int v = check_ws(workspace, workspace_bytes, kAlign);
+    if (v != LOCKS_OK) return v;
+    locks::DeviceStatus st;
+    st.word = static_cast<int32_t*>(workspace);
+    st.wait_limit_ns = limit_ns == 0 ? 1000000ull : limit_ns;
+    return cuda_status(locks::launch_wait_selftest(st, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace locks {
+
+// One thread waits on an mbarrier whose phase nothing completes (expected
+// count 2, one arrive); the bounded wait must give up and record a timeout.
+__global__ void wait_selftest_kernel(DeviceStatus st) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 2);
+        fence_barrier_init();
+        mbar_arrive(&bar);
+        if (!mbar_wait_bounded(&bar, 0, st.wait_limit_ns)) report_error(st, LOCKS_ERR_TIMEOUT);
+    }
+}
+
+cudaError_t launch_wait_selftest(DeviceStatus st, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(st);
+    return cudaGetLastError();
+}
+
+}  // namespace locks

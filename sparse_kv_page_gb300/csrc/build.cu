@@ -1,0 +1,488 @@
+// build.cu - LOCKS page-summary builder (runs when a page fills; off the
+// decode critical path).
+//
+// Per (physical page, kv head) "unit", following the LOCKS post ("How LOCKS
+// works": decomposition of the centred key deviations, int8 centroid, int4
+// rank-8 basis, int8 coefficients) and the gist.science summary 2.1 (a small
+// eigendecomposition of the centred keys):
+//   mu = mean of the 16 keys; D = K - mu;
+//   G = D D^T (16 x 16), eigenpairs by the cyclic Jacobi method in parallel
+//   (round-robin) order; the 8 largest: V[:, r] = D^T u_r / sqrt(lambda_r),
+//   C[:, r] = sqrt(lambda_r) u_r (zero if lambda_r <= 1e-12 lambda_1); the
+//   largest-magnitude entry of each V column made positive; absmax
+//   quantisation to int8 / int4 / int8 with fp16 scales, packed in the
+//   scorer's fragment order (see include/locks.h).
+//
+// GPU mapping: a warp builds two units at a time. The Gram matrix runs on the
+// tensor cores (f16 hi/lo split of the power-of-two-normalised deviations,
+// three MMAs per tile, fp32 accumulate); the Jacobi sweeps keep one row of G
+// and one row of the eigenvector matrix per lane (lanes 0-15: first unit,
+// 16-31: second), 8 disjoint rotations per round, 15 rounds per sweep, all
+// indices static (fully unrolled), operands exchanged with warp shuffles.
+#include "locks_internal.h"
+
+namespace locks {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kDStride = 136;   // fp32 row stride of D in shared memory (conflict-free float2)
+constexpr int kMaxSweeps = 10;
+
+struct WarpSmem {
+    float d[2][kPage * kDStride];
+    float mu[2][kD];
+    float g[2][kPage * kPage];
+    float u8[2][kPage * kRank];
+    float sig[2][kRank];
+    int8_t vcode[kRank * kD];
+    int8_t ccode[kPage * kRank];
+};
+
+// Round-robin pairing of 16 indices: round r pairs (r, 15) and
+// ((r + k) mod 15, (r - k) mod 15), k = 1..7.
+__host__ __device__ constexpr int pair_p(int r, int k) {
+    return k == 0 ? r : ((r + k) % 15 < (r - k + 15) % 15 ? (r + k) % 15 : (r - k + 15) % 15);
+}
+__host__ __device__ constexpr int pair_q(int r, int k) {
+    return k == 0 ? 15 : ((r + k) % 15 < (r - k + 15) % 15 ? (r - k + 15) % 15 : (r + k) % 15);
+}
+
+// Symmetric Schur rotation that zeroes a_pq (Golub & Van Loan, section 8.5).
+__device__ __forceinline__ void schur(float app, float aqq, float apq, float& c, float& s) {
+    if (fabsf(apq) <= 1e-30f || fabsf(apq) <= 1e-9f * sqrtf(fabsf(app * aqq))) {
+        c = 1.f;
+        s = 0.f;
+        return;
+    }
+    const float tau = (aqq - app) / (2.f * apq);
+    float t;
+    if (fabsf(tau) > 1e18f) {
+        t = 0.5f / tau;
+    } else {
+        t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+    }
+    c = rsqrtf(1.f + t * t);
+    s = t * c;
+}
+
+template <int R>
+__device__ __forceinline__ void jacobi_round(float (&gr)[16], float (&ur)[16], int i, int base) {
+    float c[8], s[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int P = pair_p(R, k), Q = pair_q(R, k);
+        const float app = __shfl_sync(0xffffffffu, gr[P], base + P);
+        const float aqq = __shfl_sync(0xffffffffu, gr[Q], base + Q);
+        const float apq = __shfl_sync(0xffffffffu, gr[Q], base + P);
+        schur(app, aqq, apq, c[k], s[k]);
+    }
+    // G <- G J and U <- U J (columns p, q of this lane's rows)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int P = pair_p(R, k), Q = pair_q(R, k);
+        const float gp = gr[P], gq = gr[Q];
+        gr[P] = c[k] * gp - s[k] * gq;
+        gr[Q] = s[k] * gp + c[k] * gq;
+        const float up = ur[P], uq = ur[Q];
+        ur[P] = c[k] * up - s[k] * uq;
+        ur[Q] = s[k] * up + c[k] * uq;
+    }
+    // G <- J^T G (rows p, q): combine with the partner row
+    float cm = 1.f, sm = 0.f;
+    int partner = i;
+    bool is_p = true;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int P = pair_p(R, k), Q = pair_q(R, k);
+        if (i == P) {
+            cm = c[k];
+            sm = s[k];
+            partner = Q;
+            is_p = true;
+        }
+        if (i == Q) {
+            cm = c[k];
+            sm = s[k];
+            partner = P;
+            is_p = false;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float other = __shfl_sync(0xffffffffu, gr[m], base + partner);
+        gr[m] = is_p ? (cm * gr[m] - sm * other) : (sm * other + cm * gr[m]);
+    }
+}
+
+template <int... Rs>
+struct Rounds;
+template <>
+struct Rounds<> {
+    __device__ static void run(float (&)[16], float (&)[16], int, int) {}
+};
+template <int R0, int... Rs>
+struct Rounds<R0, Rs...> {
+    __device__ static void run(float (&gr)[16], float (&ur)[16], int i, int base) {
+        jacobi_round<R0>(gr, ur, i, base);
+        Rounds<Rs...>::run(gr, ur, i, base);
+    }
+};
+
+__device__ __forceinline__ float f16_round_scale(float amax, float qmax) {
+    return __half2float(__float2half_rn(amax / qmax));
+}
+__device__ __forceinline__ int quant(float x, float s, int qmax) {
+    if (!(s > 0.f) || isinf(s)) return 0;
+    float c = rintf(x / s);
+    c = fminf(fmaxf(c, -static_cast<float>(qmax)), static_cast<float>(qmax));
+    return static_cast<int>(c);
+}
+
+// Loads a unit's keys, centres them, and forms the Gram matrix in w.g[slot].
+__device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, int slot, int lane) {
+    float* d = w.d[slot];
+    float* mu = w.mu[slot];
+    const int gid = lane >> 2, t = lane & 3;
+    if (unit >= 0) {
+        const uint16_t* src =
+            a.k_cache + (static_cast<int64_t>(a.phys_page_ids[unit / a.hkv]) * a.hkv + unit % a.hkv) * (kPage * kD);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int c = lane + 32 * m;
+            const int row = c >> 4, col = (c & 15) * 8;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + row * kD + col);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            float* dst = d + row * kDStride + col;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                dst[2 * e] = __uint_as_float(wv[e] << 16);
+                dst[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+            }
+        }
+    } else {
+        for (int idx = lane; idx < kPage * kD; idx += 32) d[(idx / kD) * kDStride + idx % kD] = 0.f;
+    }
+    __syncwarp();
+    // mean over the 16 keys, lane -> dims 4 lane .. 4 lane + 3
+    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kPage; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(d + i * kDStride + 4 * lane);
+        s4.x += v.x;
+        s4.y += v.y;
+        s4.z += v.z;
+        s4.w += v.w;
+    }
+    s4.x *= (1.f / kPage);
+    s4.y *= (1.f / kPage);
+    s4.z *= (1.f / kPage);
+    s4.w *= (1.f / kPage);
+    *reinterpret_cast<float4*>(mu + 4 * lane) = s4;
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPage; ++i) {
+        float4 v = *reinterpret_cast<const float4*>(d + i * kDStride + 4 * lane);
+        v.x -= s4.x;
+        v.y -= s4.y;
+        v.z -= s4.z;
+        v.w -= s4.w;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        *reinterpret_cast<float4*>(d + i * kDStride + 4 * lane) = v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __syncwarp();
+    // Gram on the tensor cores: D' = D * 2^-e (max |D'| < 1), split f16 hi/lo.
+    int e = 0;
+    if (amax > 0.f && amax < INFINITY) e = ilogbf(amax) + 1;
+    e = max(-100, min(100, e));
+    const float inv = __int_as_float((127 - e) << 23);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = gid + ((r & 1) ? 8 : 0);
+            const int col = 16 * s + 2 * t + ((r & 2) ? 8 : 0);
+            const float2 x = *reinterpret_cast<const float2*>(d + row * kDStride + col);
+            const uint32_t p0 = split_f16_hilo(x.x * inv), p1 = split_f16_hilo(x.y * inv);
+            hi[r] = __byte_perm(p0, p1, 0x5410);
+            lo[r] = __byte_perm(p0, p1, 0x7632);
+        }
+        // n-tile 0 = tokens 0-7 (B regs = A regs 0, 2), n-tile 1 = tokens 8-15 (A regs 1, 3)
+        mma_f16_16816(acc[0], hi, hi[0], hi[2]);
+        mma_f16_16816(acc[0], hi, lo[0], lo[2]);
+        mma_f16_16816(acc[0], lo, hi[0], hi[2]);
+        mma_f16_16816(acc[1], hi, hi[1], hi[3]);
+        mma_f16_16816(acc[1], hi, lo[1], lo[3]);
+        mma_f16_16816(acc[1], lo, hi[1], hi[3]);
+    }
+    float* g = w.g[slot];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        g[gid * kPage + nt * 8 + 2 * t] = acc[nt][0];
+        g[gid * kPage + nt * 8 + 2 * t + 1] = acc[nt][1];
+        g[(gid + 8) * kPage + nt * 8 + 2 * t] = acc[nt][2];
+        g[(gid + 8) * kPage + nt * 8 + 2 * t + 1] = acc[nt][3];
+    }
+    // the normalisation exponent travels in sig[slot][0] (as int bits) until the eigen step
+    if (lane == 0) w.sig[slot][0] = __int_as_float(e);
+    __syncwarp();
+}
+
+// Eigendecomposition of both Gram matrices (half-warp each); writes the
+// top-8 eigenvectors (columns) to u8 and sqrt(lambda) (unnormalised) to sig.
+__device__ void jacobi_top8(WarpSmem& w, int lane) {
+    const int half = lane >> 4, i = lane & 15, base = half * 16;
+    const int e = __float_as_int(w.sig[half][0]);
+    float gr[16], ur[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        gr[m] = w.g[half][i * kPage + m];
+        ur[m] = (m == i) ? 1.f : 0.f;
+    }
+    float fro2 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) fro2 += gr[m] * gr[m];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) fro2 += __shfl_xor_sync(0xffffffffu, fro2, o);
+#pragma unroll 1
+    for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
+        float off2 = 0.f, dg = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            off2 += gr[m] * gr[m];
+            dg = (m == i) ? gr[m] : dg;
+        }
+        off2 -= dg * dg;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) off2 += __shfl_xor_sync(0xffffffffu, off2, o);
+        const bool done = off2 <= 1e-13f * fro2;
+        if (__all_sync(0xffffffffu, done)) break;
+        Rounds<0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14>::run(gr, ur, i, base);
+    }
+    float lam = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) lam = (m == i) ? gr[m] : lam;
+    // rank of this eigenvalue (descending, ties -> lower index)
+    int rk = 0;
+    float lam1 = lam;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float lj = __shfl_sync(0xffffffffu, lam, base + j);
+        rk += (lj > lam) || (lj == lam && j < i);
+        lam1 = fmaxf(lam1, lj);
+    }
+    const float scale = __int_as_float((127 + e) << 23);   // 2^e: undo the Gram normalisation
+#pragma unroll
+    for (int r = 0; r < kRank; ++r) {
+        // column index (lane within the half) holding rank r
+        const unsigned bal = __ballot_sync(0xffffffffu, rk == r);
+        const int col = __ffs((bal >> base) & 0xffffu) - 1;
+        float uv = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) uv = (j == col) ? ur[j] : uv;
+        w.u8[half][i * kRank + r] = uv;
+        if (i == col) {
+            const bool dead = !(lam1 > 0.f) || lam <= 1e-12f * lam1;
+            w.sig[half][r] = dead ? 0.f : sqrtf(lam) * scale;
+        }
+    }
+    __syncwarp();
+}
+
+// V, C, quantisation and packing for one unit; writes its summary bytes.
+__device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int slot, int lane) {
+    const float* d = w.d[slot];
+    const float* u8 = w.u8[slot];
+    const float* sig = w.sig[slot];
+    // V[d][r] = sum_i D[i][d] u_r[i] / sigma_r, lane -> dims 4 lane .. +3
+    float v[4][kRank];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int r = 0; r < kRank; ++r) v[q][r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPage; ++i) {
+        const float4 dv = *reinterpret_cast<const float4*>(d + i * kDStride + 4 * lane);
+        const float4 ua = *reinterpret_cast<const float4*>(u8 + i * kRank);
+        const float4 ub = *reinterpret_cast<const float4*>(u8 + i * kRank + 4);
+        const float uu[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+        const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int r = 0; r < kRank; ++r) v[q][r] = fmaf(dd[q], uu[r], v[q][r]);
+    }
+    float flip[kRank];
+    float vmax = 0.f;
+#pragma unroll
+    for (int r = 0; r < kRank; ++r) {
+        const float inv = sig[r] > 0.f ? 1.f / sig[r] : 0.f;
+        float best = -1.f;
+        int bidx = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q][r] *= inv;
+            if (fabsf(v[q][r]) > best) {
+                best = fabsf(v[q][r]);
+                bidx = 4 * lane + q;
+            }
+        }
+        float bval = v[0][r];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bval = (4 * lane + q == bidx) ? v[q][r] : bval;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, bidx, o);
+            const float v2 = __shfl_xor_sync(0xffffffffu, bval, o);
+            if (b2 > best || (b2 == best && i2 < bidx)) {
+                best = b2;
+                bidx = i2;
+                bval = v2;
+            }
+        }
+        flip[r] = bval < 0.f ? -1.f : 1.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q][r] *= flip[r];
+            vmax = fmaxf(vmax, fabsf(v[q][r]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    const float sv = f16_round_scale(vmax, 7.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int r = 0; r < kRank; ++r) w.vcode[r * kD + 4 * lane + q] = static_cast<int8_t>(quant(v[q][r], sv, 7));
+    // C[i][r] = sigma_r u_r[i] (same sign flip); lane -> 4 of the 128 entries
+    float cv[4];
+    float cmax = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int idx = 4 * lane + q, i = idx / kRank, r = idx % kRank;
+        float fl = 1.f;
+#pragma unroll
+        for (int rr = 0; rr < kRank; ++rr) fl = (rr == r) ? flip[rr] : fl;
+        cv[q] = sig[r] * u8[i * kRank + r] * fl;
+        cmax = fmaxf(cmax, fabsf(cv[q]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+    const float sc = f16_round_scale(cmax, 127.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w.ccode[4 * lane + q] = static_cast<int8_t>(quant(cv[q], sc, 127));
+    // centroid
+    const float4 m4 = *reinterpret_cast<const float4*>(w.mu[slot] + 4 * lane);
+    float mmax = fmaxf(fmaxf(fabsf(m4.x), fabsf(m4.y)), fmaxf(fabsf(m4.z), fabsf(m4.w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    const float smu = f16_round_scale(mmax, 127.f);
+    __syncwarp();
+    if (unit < 0) return;
+
+    // pack: basis byte ob = 64 r + 16 t + 4 j + pb; low nibble h = 0, high h = 1,
+    // s = 2 j + pb % 2, e = pb / 2, dim = 16 s + 8 h + 2 t + e
+    uint32_t words[4];
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) {
+            const int ob = 16 * lane + 4 * wi + bi;
+            const int r = ob >> 6, rem = ob & 63, t = rem >> 4, j = (rem & 15) >> 2, pb = rem & 3;
+            const int s = 2 * j + (pb & 1), e = pb >> 1;
+            const int d0 = 16 * s + 2 * t + e, d1 = d0 + 8;
+            const uint32_t byte = (static_cast<uint32_t>(w.vcode[r * kD + d0]) & 0xfu) |
+                                  ((static_cast<uint32_t>(w.vcode[r * kD + d1]) & 0xfu) << 4);
+            word |= byte << (8 * bi);
+        }
+        words[wi] = word;
+    }
+    const int64_t out_unit = static_cast<int64_t>(a.phys_page_ids[unit / a.hkv]) * a.hkv + unit % a.hkv;
+    *reinterpret_cast<uint4*>(a.basis + out_unit * 512 + 16 * lane) = make_uint4(words[0], words[1], words[2], words[3]);
+    // mu byte o: t = o / 32, s = (o % 32) / 4, h = (o % 4) / 2, e = o % 2
+    {
+        uint32_t word = 0;
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) {
+            const int o = 4 * lane + bi;
+            const int t = o >> 5, s = (o & 31) >> 2, h = (o & 3) >> 1, e = o & 1;
+            const int dim = 16 * s + 8 * h + 2 * t + e;
+            const int code = quant(w.mu[slot][dim], smu, 127);
+            word |= (static_cast<uint32_t>(code) & 0xffu) << (8 * bi);
+        }
+        reinterpret_cast<uint32_t*>(a.mu + out_unit * 128)[lane] = word;
+    }
+    // coef byte o: lane' = o / 4 (gid' = lane' / 4, t' = lane' % 4), i = gid' + 8 ((o % 4) / 2), r = 2 t' + o % 2
+    {
+        uint32_t word = 0;
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) {
+            const int o = 4 * lane + bi;
+            const int lp = o >> 2, gp = lp >> 2, tp = lp & 3;
+            const int i = gp + 8 * ((o & 3) >> 1), r = 2 * tp + (o & 1);
+            word |= (static_cast<uint32_t>(w.ccode[i * kRank + r]) & 0xffu) << (8 * bi);
+        }
+        reinterpret_cast<uint32_t*>(a.coef + out_unit * 128)[lane] = word;
+    }
+    if (lane == 0) {
+        const uint32_t h0 = __half_as_ushort(__float2half_rn(smu));
+        const uint32_t h1 = __half_as_ushort(__float2half_rn(sv));
+        const uint32_t h2 = __half_as_ushort(__float2half_rn(sc));
+        *reinterpret_cast<uint2*>(a.scales + out_unit * 4) = make_uint2(h0 | (h1 << 16), h2);
+    }
+    __syncwarp();
+}
+
+// The unit index, or -1 when it does not exist or its page id is out of range
+// (then it is skipped and LOCKS_ERR_BAD_INDEX recorded).
+__device__ __forceinline__ int64_t valid_unit(const BuildArgs& a, int64_t u) {
+    if (u < 0) return -1;
+    const int phys = a.phys_page_ids[u / a.hkv];
+    if (phys < 0 || phys >= a.num_phys) {
+        if ((threadIdx.x & 31) == 0) report_error(a.st, LOCKS_ERR_BAD_INDEX);
+        return -1;
+    }
+    return u;
+}
+
+__global__ void __launch_bounds__(kThreads) build_kernel(BuildArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    WarpSmem& w = reinterpret_cast<WarpSmem*>(smem)[warp];
+    const int64_t n_units = static_cast<int64_t>(a.n_pages) * a.hkv;
+    const int64_t n_pairs = (n_units + 1) / 2;
+    for (int64_t pi = static_cast<int64_t>(blockIdx.x) * kWarps + warp; pi < n_pairs;
+         pi += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int64_t u0 = 2 * pi, u1 = (2 * pi + 1 < n_units) ? 2 * pi + 1 : -1;
+        const int64_t v0 = valid_unit(a, u0), v1 = valid_unit(a, u1);
+        load_centre_gram(a, v0, w, 0, lane);
+        load_centre_gram(a, v1, w, 1, lane);
+        jacobi_top8(w, lane);
+        finish_unit(a, v0, w, 0, lane);
+        finish_unit(a, v1, w, 1, lane);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_build(const BuildArgs& a, int num_sms, cudaStream_t stream) {
+    const int64_t n_units = static_cast<int64_t>(a.n_pages) * a.hkv;
+    if (n_units == 0) return cudaSuccess;
+    const size_t smem = kWarps * sizeof(WarpSmem);
+    cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t pairs = (n_units + 1) / 2;
+    int64_t grid = (pairs + kWarps - 1) / kWarps;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 2;
+    if (grid > cap) grid = cap;
+    build_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace locks

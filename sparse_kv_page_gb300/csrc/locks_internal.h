@@ -1,0 +1,69 @@
+// locks_internal.h - launchers shared between the kernel files and the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "locks_common.cuh"
+
+namespace locks {
+
+struct ScoreArgs {
+    const float* q;
+    const int8_t* mu;
+    const uint8_t* basis;
+    const int8_t* coef;
+    const uint16_t* scales;
+    const int32_t* page_table;
+    const int32_t* seq_pages;
+    float* scores;
+    int batch, hq, hkv, max_pages, num_phys;
+    DeviceStatus st;
+};
+cudaError_t launch_score(const ScoreArgs& a, int num_sms, cudaStream_t stream);
+
+struct SelectAttendArgs {
+    // selection
+    const float* scores;
+    const int32_t* seq_pages;
+    int32_t* selected;        // [B][Hkv][k_cap]
+    int32_t* n_selected;      // [B][Hkv]
+    float* sel_keys;          // nullable
+    int budget_pages;         // budget_tokens / 16
+    int k_cap;
+    // attention
+    const float* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* page_table;
+    uint16_t* out;
+    float* lse;               // nullable
+    int batch, hq, hkv, max_pages, num_phys;
+    DeviceStatus st;
+};
+enum class SAMode { kSelect, kAttend, kSelectAttend };
+cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream);
+// Largest cluster size (16 or 8) the select/attend kernels can be launched with.
+int select_attend_cluster_size(int max_pages, SAMode mode);
+size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode);
+
+struct BuildArgs {
+    const uint16_t* k_cache;
+    const int32_t* phys_page_ids;
+    int n_pages;
+    int hkv;
+    int num_phys;
+    int8_t* mu;
+    uint8_t* basis;
+    int8_t* coef;
+    uint16_t* scales;
+    DeviceStatus st;
+};
+cudaError_t launch_build(const BuildArgs& a, int num_sms, cudaStream_t stream);
+
+// Bounded-wait self test: one CTA waits on an mbarrier phase that never
+// completes and must give up after the limit, recording LOCKS_ERR_TIMEOUT.
+cudaError_t launch_wait_selftest(DeviceStatus st, cudaStream_t stream);
+
+}  // namespace locks

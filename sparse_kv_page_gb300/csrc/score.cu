@@ -1,0 +1,307 @@
+// score.cu - LOCKS page scoring from the resident summaries alone.
+//
+// Computes, for every (sequence b, query head h, logical page j), the score of
+// the LOCKS post ("How LOCKS works") and of the gist.science summary, 2.2:
+//     s = log sum_{i<16} exp[(q . mu + (V^T q) . c_i) / sqrt(128)]
+// from the int8 centroid, int4 rank-8 basis and int8 coefficients of unit
+// (page_table[b][j], h / g). No key or value is read.
+//
+// Design (HBM-bound stream of 776 B per unit):
+//  * persistent CTAs, one per SM; a producer warp streams the summaries of
+//    64 units per stage (all kv heads of 64/Hkv consecutive logical pages)
+//    into a 4-stage shared-memory ring with bulk async copies (TMA engine,
+//    L2 evict-first) plus 8-byte LDGSTS for the fp16 scales, completion on
+//    mbarriers; 8 consumer warps each own one kv head and 8 pages per stage.
+//  * V^T q and mu . q run on the tensor cores (mma.sync m16n8k16, f16 in,
+//    fp32 accumulate): A = int4/int8 codes (exact in f16), B = the query
+//    split into an f16 high and low part (about 22 significant bits), so the
+//    products match fp32 arithmetic to well below the 1e-3 score tolerance.
+//    The query is pre-scaled by a power of two per head so the f16 parts
+//    never overflow.
+//  * the per-token reconstruction (V^T q) . c_i is a second MMA (m16n8k8)
+//    whose B operand is the first MMA's accumulator, split hi/lo and
+//    transposed in registers with movmatrix; the page LSE is a 3-step
+//    butterfly over the 8 lanes that hold the 16 token logits.
+#include "locks_internal.h"
+
+namespace locks {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStageUnits = 64;
+constexpr int kStages = 4;
+constexpr int kStMu = 0;
+constexpr int kStBasis = kStMu + kStageUnits * 128;
+constexpr int kStCoef = kStBasis + kStageUnits * 512;
+constexpr int kStScales = kStCoef + kStageUnits * 128;
+constexpr int kStageBytes = kStScales + kStageUnits * 8;   // 49,664 B
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStages * 8;
+
+__device__ __forceinline__ float pow2i(int e) {  // 2^e for |e| <= 126
+    return __int_as_float((127 + e) << 23);
+}
+
+template <int HKV, int NT>
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nchunks, int total_items) {
+    constexpr int NP = kStageUnits / HKV;   // pages per stage
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* empty = full + kStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 33);              // 1 expect_tx arrive + 32 LDGSTS arrives
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int per = (total_items + gridDim.x - 1) / gridDim.x;
+    const int it0 = blockIdx.x * per;
+    const int it1 = min(total_items, it0 + per);
+    bool failed = false;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        const uint64_t pol = policy_evict_first();
+        uint32_t k = 0;
+        bool bad = false;
+        for (int it = it0; it < it1; ++it) {
+            const int b = it / nchunks, page0 = (it % nchunks) * NP;
+            const int nvalid = min(NP, min(a.seq_pages[b], a.max_pages) - page0);
+            if (nvalid <= 0) continue;
+            const int s = k % kStages;
+            if (!mbar_wait_bounded(&empty[s], ((k / kStages) & 1) ^ 1, a.st.wait_limit_ns)) failed = true;
+            uint8_t* stg = smem + s * kStageBytes;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nvalid * HKV * 768));
+            __syncwarp();
+            for (int pg = lane; pg < nvalid; pg += 32) {
+                int64_t phys = a.page_table[static_cast<int64_t>(b) * a.max_pages + page0 + pg];
+                if (phys < 0 || phys >= a.num_phys) {
+                    bad = true;
+                    phys = 0;
+                }
+                const int64_t u0 = phys * HKV;
+                bulk_g2s_hint(stg + kStMu + pg * HKV * 128, a.mu + u0 * 128, HKV * 128, &full[s], pol);
+                bulk_g2s_hint(stg + kStBasis + pg * HKV * 512, a.basis + u0 * 512, HKV * 512, &full[s], pol);
+                bulk_g2s_hint(stg + kStCoef + pg * HKV * 128, a.coef + u0 * 128, HKV * 128, &full[s], pol);
+#pragma unroll
+                for (int h = 0; h < HKV; ++h)
+                    cp_async_8(stg + kStScales + (pg * HKV + h) * 8, a.scales + (u0 + h) * 4);
+            }
+            cp_async_arrive_noinc(&full[s]);
+            ++k;
+        }
+        if (bad) report_error(a.st, LOCKS_ERR_BAD_INDEX);
+    } else {
+        // ------------------------------------------------------ consumers
+        const int kvh = warp % HKV, blk = warp / HKV;
+        const int gid = lane >> 2, t = lane & 3;
+        const int g = a.hq / HKV;
+        uint32_t bq[8][NT][2];
+        float qsc[NT];     // 2^e of the output head (4 nt + t) of this thread
+        int cur_b = -1;
+        uint32_t k = 0;
+        for (int it = it0; it < it1; ++it) {
+            const int b = it / nchunks, page0 = (it % nchunks) * NP;
+            const int nvalid = min(NP, min(a.seq_pages[b], a.max_pages) - page0);
+            if (nvalid <= 0) continue;
+            if (b != cur_b) {
+                // Per-head power-of-two pre-scale: max |q'| < 1.
+                int eB[NT], eO[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) eB[nt] = eO[nt] = 0;
+#pragma unroll
+                for (int hh = 0; hh < 4 * NT; ++hh) {
+                    float mx = 0.f;
+                    if (hh < g) {
+                        const float4 v = *reinterpret_cast<const float4*>(
+                            a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * kD + lane * 4);
+                        mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    int e = 0;
+                    if (mx > 0.f && mx < INFINITY) e = ilogbf(mx) + 1;
+                    e = max(-100, min(100, e));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (((nt * 8 + gid) >> 1) == hh) eB[nt] = e;
+                        if (4 * nt + t == hh) eO[nt] = e;
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    qsc[nt] = pow2i(eO[nt]);
+                    const int col = nt * 8 + gid, hh = col >> 1, hl = col & 1;
+                    const float inv = pow2i(-eB[nt]);
+                    const float* qrow = a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * kD;
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        uint32_t r0 = 0, r1 = 0;
+                        if (hh < g) {
+                            const float2 x01 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t);
+                            const float2 x89 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t + 8);
+                            const uint32_t p0 = split_f16_hilo(x01.x * inv), p1 = split_f16_hilo(x01.y * inv);
+                            const uint32_t p8 = split_f16_hilo(x89.x * inv), p9 = split_f16_hilo(x89.y * inv);
+                            // hl = 0: high parts (low halves), hl = 1: low parts (high halves)
+                            r0 = hl ? __byte_perm(p0, p1, 0x7632) : __byte_perm(p0, p1, 0x5410);
+                            r1 = hl ? __byte_perm(p8, p9, 0x7632) : __byte_perm(p8, p9, 0x5410);
+                        }
+                        bq[s][nt][0] = r0;
+                        bq[s][nt][1] = r1;
+                    }
+                }
+                cur_b = b;
+            }
+            const int s = k % kStages;
+            if (!mbar_wait_bounded(&full[s], (k / kStages) & 1, a.st.wait_limit_ns)) failed = true;
+            const uint8_t* stg = smem + s * kStageBytes;
+            const int nv = min(8, nvalid - 8 * blk);
+            if (nv > 0) {
+                const int ubase = (8 * blk) * HKV + kvh;   // stage unit index of the warp's unit 0
+                // scales of unit `lane` (lanes 0..7); zero for units past the end
+                float s_mu = 0.f, s_v = 0.f, s_c = 0.f;
+                if (lane < nv) {
+                    const uint2 sc = *reinterpret_cast<const uint2*>(stg + kStScales + (ubase + lane * HKV) * 8);
+                    s_mu = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x & 0xffffu)));
+                    s_v = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x >> 16)));
+                    s_c = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.y & 0xffffu)));
+                }
+                // centroid term: rows = the warp's 8 units, K = 128 dims
+                float accmu[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) accmu[nt][0] = accmu[nt][1] = accmu[nt][2] = accmu[nt][3] = 0.f;
+                {
+                    const uint8_t* mrow = stg + kStMu + (ubase + gid * HKV) * 128 + t * 32;
+                    const uint4 m0 = *reinterpret_cast<const uint4*>(mrow);
+                    const uint4 m1 = *reinterpret_cast<const uint4*>(mrow + 16);
+                    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint32_t lo, hi;
+                        int8x4_to_f16x2(mw[ks], lo, hi);
+                        const uint32_t af[4] = {lo, 0u, hi, 0u};
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(accmu[nt], af, bq[ks][nt][0], bq[ks][nt][1]);
+                    }
+                }
+                const float smu_row = __shfl_sync(0xffffffffu, s_mu, gid);
+                float score_out[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) score_out[nt] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // MMA1 rows 0-7: ranks of unit i, rows 8-15: ranks of unit i + 4
+                    const uint4 va = *reinterpret_cast<const uint4*>(stg + kStBasis + (ubase + i * HKV) * 512 + lane * 16);
+                    const uint4 vb =
+                        *reinterpret_cast<const uint4*>(stg + kStBasis + (ubase + (i + 4) * HKV) * 512 + lane * 16);
+                    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+                    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+                    float acc[NT][4];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t ra[4], rb[4];
+                        int4x8_to_f16x2(wa[j], ra);
+                        int4x8_to_f16x2(wb[j], rb);
+                        const uint32_t a0[4] = {ra[0], rb[0], ra[1], rb[1]};   // k-step 2j
+                        const uint32_t a1[4] = {ra[2], rb[2], ra[3], rb[3]};   // k-step 2j + 1
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_f16_16816(acc[nt], a0, bq[2 * j][nt][0], bq[2 * j][nt][1]);
+                            mma_f16_16816(acc[nt], a1, bq[2 * j + 1][nt][0], bq[2 * j + 1][nt][1]);
+                        }
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int u = i + 4 * half;
+                        const float svu = __shfl_sync(0xffffffffu, s_v, u);
+                        const float fc = __shfl_sync(0xffffffffu, s_c, u) * (kInvSqrtD * kLog2e);
+                        const uint32_t cw =
+                            *reinterpret_cast<const uint32_t*>(stg + kStCoef + (ubase + u * HKV) * 128 + lane * 4);
+                        uint32_t ca0, ca1;
+                        int8x4_to_f16x2(cw, ca0, ca1);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const float w = (half == 0 ? acc[nt][0] + acc[nt][1] : acc[nt][2] + acc[nt][3]) * svu;
+                            const uint32_t bw = movmatrix_trans(split_f16_hilo(w));
+                            float d2[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma_f16_1688(d2, ca0, ca1, bw);
+                            const float f = fc * qsc[nt];
+                            const float x0 = (d2[0] + d2[1]) * f;
+                            const float x1 = (d2[2] + d2[3]) * f;
+                            float m = fmaxf(x0, x1);
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            float z = fast_exp2(x0 - m) + fast_exp2(x1 - m);
+                            z += __shfl_xor_sync(0xffffffffu, z, 4);
+                            z += __shfl_xor_sync(0xffffffffu, z, 8);
+                            z += __shfl_xor_sync(0xffffffffu, z, 16);
+                            const float lse_dev = (m + fast_log2(z)) * kLn2;
+                            if (gid == u) {
+                                const float a_term = (accmu[nt][0] + accmu[nt][1]) * smu_row * qsc[nt] * kInvSqrtD;
+                                score_out[nt] = a_term + lse_dev;
+                            }
+                        }
+                    }
+                }
+                if (gid < nv) {
+                    const int page = page0 + 8 * blk + gid;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int hh = 4 * nt + t;
+                        if (hh < g)
+                            a.scores[(static_cast<int64_t>(b) * a.hq + kvh * g + hh) * a.max_pages + page] =
+                                score_out[nt];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            ++k;
+        }
+    }
+    if (failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
+}
+
+template <int HKV, int NT>
+cudaError_t launch_t(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
+    constexpr int NP = kStageUnits / HKV;
+    const int nchunks = (a.max_pages + NP - 1) / NP;
+    const int total = a.batch * nchunks;
+    if (total == 0) return cudaSuccess;
+    auto kern = score_kernel<HKV, NT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = min(total, num_sms);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(a, nchunks, total);
+    return cudaGetLastError();
+}
+
+template <int HKV>
+cudaError_t launch_h(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
+    const int g = a.hq / a.hkv;
+    if (g <= 4) return launch_t<HKV, 1>(a, num_sms, stream);
+    if (g <= 8) return launch_t<HKV, 2>(a, num_sms, stream);
+    return launch_t<HKV, 4>(a, num_sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_score(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
+    switch (a.hkv) {
+        case 1: return launch_h<1>(a, num_sms, stream);
+        case 2: return launch_h<2>(a, num_sms, stream);
+        case 4: return launch_h<4>(a, num_sms, stream);
+        case 8: return launch_h<8>(a, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace locks

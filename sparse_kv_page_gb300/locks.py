@@ -1,0 +1,252 @@
+"""Python binding of the LOCKS C ABI (include/locks.h).
+
+Argument marshalling only: every function below calls the entry point of the
+same name in ``liblocks_gb300.so`` with raw device pointers taken from torch
+tensors, on torch's current CUDA stream unless a stream is given. Nothing here
+computes any part of the method, and there is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PAGE = 16
+D_HEAD = 128
+RANK = 8
+
+_STATUS = {
+    0: "LOCKS_OK", -1: "LOCKS_ERR_INVALID_ARG", -2: "LOCKS_ERR_UNSUPPORTED",
+    -3: "LOCKS_ERR_WORKSPACE_TOO_SMALL", -4: "LOCKS_ERR_CUDA", -5: "LOCKS_ERR_TIMEOUT",
+    -6: "LOCKS_ERR_BAD_INDEX",
+}
+LOCKS_OK, LOCKS_ERR_INVALID_ARG, LOCKS_ERR_UNSUPPORTED = 0, -1, -2
+LOCKS_ERR_WORKSPACE_TOO_SMALL, LOCKS_ERR_CUDA, LOCKS_ERR_TIMEOUT, LOCKS_ERR_BAD_INDEX = -3, -4, -5, -6
+
+
+class LocksError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {status} ({_STATUS.get(status, 'unknown')})")
+        self.status = status
+
+
+class locks_dims_t(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("num_phys_pages", ctypes.c_int32)]
+
+
+class locks_summaries_t(ctypes.Structure):
+    _fields_ = [("mu", ctypes.c_void_p), ("basis", ctypes.c_void_p), ("coef", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the in-tree CUDA library; raise if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"LOCKS CUDA library not built: {path} (run __graft_entry__.build())")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, S, I32, U64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_uint64
+        D = ctypes.POINTER(locks_dims_t)
+        SUM = locks_summaries_t
+        sig = {
+            "locks_version": ([], ctypes.c_int),
+            "locks_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "locks_k_cap": ([D, I32, ctypes.POINTER(I32)], ctypes.c_int),
+            "locks_workspace_size": ([D, I32, ctypes.POINTER(S)], ctypes.c_int),
+            "locks_build_summaries": ([D, P, P, I32, SUM, P, S, P], ctypes.c_int),
+            "locks_score_pages": ([D, P, SUM, P, P, P, P, S, P], ctypes.c_int),
+            "locks_select_pages": ([D, P, P, I32, P, P, P, P, S, P], ctypes.c_int),
+            "locks_sparse_attention": ([D, P, P, P, P, P, P, I32, P, P, P, S, P], ctypes.c_int),
+            "locks_select_attend": ([D, P, P, P, P, P, P, I32, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_decode_step": ([D, P, P, P, SUM, P, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_get_device_status": ([P, ctypes.POINTER(I32), P], ctypes.c_int),
+            "locks_clear_device_status": ([P, P], ctypes.c_int),
+            "locks_set_wait_limit_ns": ([U64], ctypes.c_int),
+            "locks_selftest_bounded_wait": ([P, S, U64, P], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise LocksError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("LOCKS buffers must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------------ dims, buffers
+
+def make_dims(batch: int, num_q_heads: int, num_kv_heads: int, max_pages_per_seq: int,
+              num_phys_pages: int) -> locks_dims_t:
+    return locks_dims_t(batch, num_q_heads, num_kv_heads, D_HEAD, PAGE, RANK, max_pages_per_seq, num_phys_pages)
+
+
+@dataclasses.dataclass
+class Summaries:
+    """Device summary arrays (torch-owned) in the library's layout."""
+
+    mu: torch.Tensor       # int8  [num_phys][Hkv][128]
+    basis: torch.Tensor    # uint8 [num_phys][Hkv][512]
+    coef: torch.Tensor     # int8  [num_phys][Hkv][128]
+    scales: torch.Tensor   # int16 (fp16 bits) [num_phys][Hkv][4]
+
+    @staticmethod
+    def empty(num_phys: int, num_kv_heads: int, device="cuda") -> "Summaries":
+        return Summaries(torch.zeros((num_phys, num_kv_heads, 128), dtype=torch.int8, device=device),
+                         torch.zeros((num_phys, num_kv_heads, 512), dtype=torch.uint8, device=device),
+                         torch.zeros((num_phys, num_kv_heads, 128), dtype=torch.int8, device=device),
+                         torch.zeros((num_phys, num_kv_heads, 4), dtype=torch.int16, device=device))
+
+    def c(self) -> locks_summaries_t:
+        return locks_summaries_t(_ptr(self.mu), _ptr(self.basis), _ptr(self.coef), _ptr(self.scales))
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.mu, self.basis, self.coef, self.scales))
+
+
+def locks_version() -> int:
+    return load_library().locks_version()
+
+
+def locks_status_string(status: int) -> str:
+    return load_library().locks_status_string(status).decode()
+
+
+def locks_k_cap(dims: locks_dims_t, budget_tokens: int) -> int:
+    out = ctypes.c_int32(0)
+    _check("locks_k_cap", load_library().locks_k_cap(ctypes.byref(dims), budget_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def locks_workspace_size(dims: locks_dims_t, budget_tokens: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("locks_workspace_size",
+           load_library().locks_workspace_size(ctypes.byref(dims), budget_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def alloc_workspace(dims: locks_dims_t, budget_tokens: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace of locks_workspace_size bytes (torch allocations are 256-byte aligned)."""
+    n = locks_workspace_size(dims, budget_tokens)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def _ws(workspace: Optional[torch.Tensor]):
+    if workspace is None:
+        return None, 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+# ------------------------------------------------------------ entry points
+
+def locks_build_summaries(dims, k_cache, phys_page_ids, n_pages, summaries: Summaries, workspace=None,
+                          stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_build_summaries", load_library().locks_build_summaries(
+        ctypes.byref(dims), _ptr(k_cache), _ptr(phys_page_ids), int(n_pages), summaries.c(), ws, nws,
+        _stream(stream)))
+
+
+def locks_score_pages(dims, q, summaries: Summaries, page_table, seq_pages, scores, workspace=None,
+                      stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_score_pages", load_library().locks_score_pages(
+        ctypes.byref(dims), _ptr(q), summaries.c(), _ptr(page_table), _ptr(seq_pages), _ptr(scores), ws, nws,
+        _stream(stream)))
+
+
+def locks_select_pages(dims, scores, seq_pages, budget_tokens, selected, n_selected, sel_keys=None,
+                       workspace=None, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_select_pages", load_library().locks_select_pages(
+        ctypes.byref(dims), _ptr(scores), _ptr(seq_pages), int(budget_tokens), _ptr(selected), _ptr(n_selected),
+        _ptr(sel_keys), ws, nws, _stream(stream)))
+
+
+def locks_sparse_attention(dims, q, k_cache, v_cache, page_table, selected, n_selected, k_cap, out, lse=None,
+                           workspace=None, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_sparse_attention", load_library().locks_sparse_attention(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(selected),
+        _ptr(n_selected), int(k_cap), _ptr(out), _ptr(lse), ws, nws, _stream(stream)))
+
+
+def locks_select_attend(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
+                        n_selected, out, lse=None, workspace=None, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_select_attend", load_library().locks_select_attend(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(scores), _ptr(seq_pages),
+        int(budget_tokens), _ptr(selected), _ptr(n_selected), _ptr(out), _ptr(lse), ws, nws, _stream(stream)))
+
+
+def locks_decode_step(dims, q, k_cache, v_cache, summaries: Summaries, page_table, seq_pages, budget_tokens, out,
+                      workspace, lse=None, scores=None, selected=None, n_selected=None, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_decode_step", load_library().locks_decode_step(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), summaries.c(), _ptr(page_table),
+        _ptr(seq_pages), int(budget_tokens), _ptr(out), _ptr(lse), _ptr(scores), _ptr(selected),
+        _ptr(n_selected), ws, nws, _stream(stream)))
+
+
+def locks_get_device_status(workspace, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check("locks_get_device_status",
+           load_library().locks_get_device_status(_ptr(workspace), ctypes.byref(out), _stream(stream)))
+    return out.value
+
+
+def locks_clear_device_status(workspace, stream=None) -> None:
+    _check("locks_clear_device_status", load_library().locks_clear_device_status(_ptr(workspace), _stream(stream)))
+
+
+def locks_set_wait_limit_ns(ns: int) -> None:
+    _check("locks_set_wait_limit_ns", load_library().locks_set_wait_limit_ns(int(ns)))
+
+
+def locks_selftest_bounded_wait(workspace, limit_ns: int, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_selftest_bounded_wait",
+           load_library().locks_selftest_bounded_wait(ws, nws, int(limit_ns), _stream(stream)))
