@@ -234,30 +234,75 @@ class DecodeInputs:
     types: List[List[np.ndarray]]     # [b][kvh] -> page types
 
 
-def make_decode_inputs(w: Workload, with_values: bool = True) -> DecodeInputs:
-    """Generate the full paged K/V cache, queries and page table of a workload."""
+def _fill_chunk(w: Workload, b: int, kvh: int, p0: int, k_cache: np.ndarray, v_cache: Optional[np.ndarray],
+                table: np.ndarray, q: np.ndarray) -> None:
+    p1 = min(w.pages, p0 + CHUNK_PAGES)
+    types = page_types(w, b, kvh)
+    car = carrier_pages(w, b, kvh, q[b])
+    phys = table[b, p0:p1]
+    k_cache[phys, kvh] = f32_to_bf16_bits(make_keys_chunk(w, b, kvh, p0, p1, types, car))
+    if v_cache is not None:
+        v_cache[phys, kvh] = f32_to_bf16_bits(make_values_chunk(w, b, kvh, p0, p1))
+
+
+def _chunk_task(args) -> None:
+    """Worker body: attach to the shared K/V buffers and fill one (b, kv head, chunk)."""
+    from multiprocessing import shared_memory
+    w, b, kvh, p0, k_name, v_name, shape = args
+    shm_k = shared_memory.SharedMemory(name=k_name)
+    shm_v = shared_memory.SharedMemory(name=v_name) if v_name else None
+    try:
+        k = np.ndarray(shape, dtype=np.uint16, buffer=shm_k.buf)
+        v = np.ndarray(shape, dtype=np.uint16, buffer=shm_v.buf) if shm_v else None
+        _fill_chunk(w, b, kvh, p0, k, v, make_page_table(w), make_queries(w))
+        del k, v
+    finally:
+        shm_k.close()
+        if shm_v:
+            shm_v.close()
+
+
+def make_decode_inputs(w: Workload, with_values: bool = True, workers: int = 0) -> DecodeInputs:
+    """Generate the full paged K/V cache, queries and page table of a workload.
+
+    Each (request, kv head, chunk of pages) has its own random stream, so the
+    result does not depend on ``workers``; with workers > 1 the chunks are
+    generated by a spawn-started process pool writing into shared memory.
+    """
     q = make_queries(w)
     table = make_page_table(w)
     shape = (w.num_phys_pages, w.num_kv_heads, PAGE, D_HEAD)
-    k_cache = np.empty(shape, dtype=np.uint16)
-    v_cache = np.empty(shape, dtype=np.uint16) if with_values else np.zeros((0,), np.uint16)
-    carriers: List[List[np.ndarray]] = []
-    types_all: List[List[np.ndarray]] = []
-    for b in range(w.batch):
-        crow, trow = [], []
-        for kvh in range(w.num_kv_heads):
-            types = page_types(w, b, kvh)
-            car = carrier_pages(w, b, kvh, q[b])
-            crow.append(car[0])
-            trow.append(types)
-            for p0 in range(0, w.pages, CHUNK_PAGES):
-                p1 = min(w.pages, p0 + CHUNK_PAGES)
-                phys = table[b, p0:p1]
-                k_cache[phys, kvh] = f32_to_bf16_bits(make_keys_chunk(w, b, kvh, p0, p1, types, car))
-                if with_values:
-                    v_cache[phys, kvh] = f32_to_bf16_bits(make_values_chunk(w, b, kvh, p0, p1))
-        carriers.append(crow)
-        types_all.append(trow)
+    tasks = [(b, kvh, p0) for b in range(w.batch) for kvh in range(w.num_kv_heads)
+             for p0 in range(0, w.pages, CHUNK_PAGES)]
+    if workers > 1 and len(tasks) > 1:
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        nbytes = int(np.prod(shape)) * 2
+        shm_k = shared_memory.SharedMemory(create=True, size=nbytes)
+        shm_v = shared_memory.SharedMemory(create=True, size=nbytes) if with_values else None
+        try:
+            args = [(w, b, kvh, p0, shm_k.name, shm_v.name if shm_v else None, shape) for b, kvh, p0 in tasks]
+            from concurrent.futures import ProcessPoolExecutor
+            # spawn (not fork: callers may already hold a CUDA context); a worker
+            # that dies raises BrokenProcessPool instead of being respawned
+            with ProcessPoolExecutor(min(workers, len(tasks)), mp_context=mp.get_context("spawn")) as ex:
+                list(ex.map(_chunk_task, args))
+            k_cache = np.ndarray(shape, dtype=np.uint16, buffer=shm_k.buf).copy()
+            v_cache = (np.ndarray(shape, dtype=np.uint16, buffer=shm_v.buf).copy() if shm_v
+                       else np.zeros((0,), np.uint16))
+        finally:
+            shm_k.close()
+            shm_k.unlink()
+            if shm_v:
+                shm_v.close()
+                shm_v.unlink()
+    else:
+        k_cache = np.empty(shape, dtype=np.uint16)
+        v_cache = np.empty(shape, dtype=np.uint16) if with_values else np.zeros((0,), np.uint16)
+        for b, kvh, p0 in tasks:
+            _fill_chunk(w, b, kvh, p0, k_cache, v_cache if with_values else None, table, q)
+    carriers = [[carrier_pages(w, b, kvh, q[b])[0] for kvh in range(w.num_kv_heads)] for b in range(w.batch)]
+    types_all = [[page_types(w, b, kvh) for kvh in range(w.num_kv_heads)] for b in range(w.batch)]
     seq_pages = np.full(w.batch, w.pages, dtype=np.int32)
     return DecodeInputs(w, q, k_cache, v_cache, table, seq_pages, carriers, types_all)
 

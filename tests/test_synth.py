@@ -57,3 +57,10 @@ def test_random_summaries_valid_codes():
     assert s.mu.min() >= -127 and s.coef.min() >= -127
     sc = s.scales.view(np.float16).astype(np.float64)
     assert np.all(sc[..., :3] > 0) and np.all(sc[..., 3] == 0)
+
+
+def test_parallel_generation_matches_serial():
+    w = synth.WORKLOADS["batch8_256k"].scaled(pages=5000, batch=2)
+    a = synth.make_decode_inputs(w)
+    b = synth.make_decode_inputs(w, workers=3)
+    assert np.array_equal(a.k_cache, b.k_cache) and np.array_equal(a.v_cache, b.v_cache)
