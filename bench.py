@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""LOCKS decode-step benchmark on GB300.
+
+One step = one pass of the whole decode hot path over one batch: summary-only
+page scoring of every page, group-shared top-k selection, and sparse attention
+over the kept pages (the two kernels ``locks_decode_step`` launches, called here
+as ``locks_score_pages`` + ``locks_select_attend`` so that the scoring kernel can
+be bracketed by CUDA events inside the timed region).
+
+Default workload: the 1M-token context, batch 1, 32 query / 8 kv heads,
+budget 2048 tokens (``--workload`` / ``--budget`` select the others). Inputs
+are synthetic (the seeded generator in ``synth``) and resident in HBM when the
+timed region starts; L2 is flushed (512 MiB write) between timed steps.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the float64 CPU
+oracle on the host cores instead (the reference arm of this project).
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(the step has no cross-request exchange); timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode-step µs and effective HBM GB/s (% of GB300 roofline) at 128K–1M ctx"
+UNIT_BYTES = 776                 # summary bytes per (page, kv head)
+PAGE_KV_BYTES = 2 * 16 * 128 * 2  # K + V bytes per (page, kv head)
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29533")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML (read-only) in a thread."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, uuid: str | None, period_s: float = 0.002):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            r = -1
+            if uuid:
+                r = self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+            if r != 0:
+                idx = int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0)
+                r = self.nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h))
+            if r != 0:
+                return
+            mx = ctypes.c_uint()
+            rc = self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = float(mx.value) if rc == 0 else None
+            fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self._reasons_fn = fn or self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _one(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        pw = ctypes.c_uint()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        self._reasons_fn(self.h, ctypes.byref(rs))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        self.samples.append((float(clk.value), int(rs.value), pw.value / 1000.0))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._one()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._loop, daemon=True)
+            self._t.start()
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+            self._one()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        clocks = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[1]
+        reasons = [name for bit, name in self.REASONS.items() if bits & bit]
+        return {"sm_mhz": statistics.median(clocks), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "power_w_max": max(s[2] for s in self.samples)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from sparse_kv_page_gb300 import build as B
+    ent = rec.get(kernel)
+    if not ent or ent.get("source_fingerprint") != B._fingerprint()[:16]:
+        return None
+    return ent
+
+
+# ----------------------------------------------------------------- workload
+
+def workload_of(args) -> tuple[synth.Workload, int]:
+    w = synth.WORKLOADS[args.workload]
+    budget = args.budget if args.budget is not None else max(w.budgets)
+    return w, budget
+
+
+def algorithmic_bytes(w: synth.Workload, budget: int) -> tuple[int, int]:
+    units = w.batch * w.pages * w.num_kv_heads
+    k = min(budget // 16, w.pages)
+    return units * UNIT_BYTES, w.batch * w.num_kv_heads * k * PAGE_KV_BYTES
+
+
+def config_of(w: synth.Workload, budget: int) -> dict:
+    return {"workload": f"{w.name}: {w.description}", "batch": w.batch, "context_tokens": w.context,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": 16,
+            "rank": 8, "budget_tokens": budget, "pages_per_seq": w.pages,
+            "l2": "flushed between timed steps (512 MiB write, outside the step events)"}
+
+
+# ---------------------------------------------------------- oracle (CPU) arm
+
+class OracleStep:
+    """The float64 oracle's decode step on one (request, kv head) segment per call.
+
+    A full step is every segment; one call times one segment (scores of all its
+    pages for the group's query heads, group keys, selection, attention) and the
+    per-step figure is that time times the number of segments, so a step stays
+    bounded. Summary bytes are random (the oracle's cost does not depend on
+    their values)."""
+
+    def __init__(self, w: synth.Workload, budget: int, inp: synth.DecodeInputs):
+        import oracle
+        oracle.build()
+        self.o = oracle
+        self.w, self.budget, self.inp = w, budget, inp
+        s = synth.random_summaries(w.num_phys_pages, w.num_kv_heads, seed=12345)
+        self.seg = []
+        for b in range(w.batch):
+            for kvh in range(w.num_kv_heads):
+                self.seg.append((b, kvh))
+        self.per_kvh = [tuple(np.ascontiguousarray(a[:, kvh:kvh + 1]) for a in (s.mu, s.basis, s.coef, s.scales))
+                        for kvh in range(w.num_kv_heads)]
+        self.i = 0
+
+    def run_one(self) -> float:
+        """Seconds for one segment."""
+        w, o = self.w, self.o
+        b, kvh = self.seg[self.i % len(self.seg)]
+        self.i += 1
+        g = w.group
+        q = np.ascontiguousarray(self.inp.q[b:b + 1, kvh * g:(kvh + 1) * g])
+        table = np.ascontiguousarray(self.inp.page_table[b:b + 1])
+        seq = self.inp.seq_pages[b:b + 1]
+        mu, basis, coef, scales = self.per_kvh[kvh]
+        t0 = time.perf_counter()
+        s = o.scores(q, mu, basis, coef, scales, table, seq, 1)
+        keys, _ = o.group_keys(s, seq, 1)
+        sel, nsel = o.select(keys, seq, self.budget)
+        t1 = time.perf_counter()
+        full_sel = np.zeros((1, w.num_kv_heads, sel.shape[2]), np.int32)
+        full_n = np.zeros((1, w.num_kv_heads), np.int32)
+        full_sel[0, kvh] = sel[0, 0]
+        full_n[0, kvh] = nsel[0, 0]
+        qb = np.ascontiguousarray(self.inp.q[b:b + 1])
+        t2 = time.perf_counter()
+        o.attend(qb, self.inp.k_cache, self.inp.v_cache, table, full_sel, full_n)
+        t3 = time.perf_counter()
+        return (t1 - t0) + (t3 - t2)
+
+    @property
+    def segments(self) -> int:
+        return len(self.seg)
+
+    def cores(self) -> int:
+        return self.o.max_threads()
+
+
+def cpu_baseline(step: OracleStep, budget_s: float = 12.0, max_calls: int = 64) -> dict:
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < max_calls and (not times or time.perf_counter() < t_end):
+        times.append(step.run_one())
+    per_step_us = statistics.mean(times) * step.segments * 1e6
+    return {"value": per_step_us, "unit": "us", "cores": step.cores(), "kind": "oracle",
+            "sample": f"{len(times)} of the step's {step.segments} (request, kv head) segments, each fully "
+                      f"scored/selected/attended in float64; per-step time = mean segment time x segments; "
+                      f"random summary bytes of the same shape"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w, budget = workload_of(args)
+    inp = synth.make_decode_inputs(w, workers=min(16, os.cpu_count() or 1))
+    step = OracleStep(w, budget, inp)
+    for _ in range(args.warmup):
+        step.run_one()
+    times = [step.run_one() * step.segments * 1e6 for _ in range(args.steps)]
+    value = statistics.mean(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "us", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, budget),
+            "cpu_baseline": {"value": value, "unit": "us", "cores": step.cores(), "kind": "oracle",
+                             "sample": f"each step = one (request, kv head) segment of {step.segments}, "
+                                       f"extrapolated x{step.segments}"},
+            "e2e": {"value": value, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- GPU arm
+
+def run_locks(args, rank, world, local):
+    w, budget = workload_of(args)
+    workers = min(16, os.cpu_count() or 1)
+    inp = synth.make_decode_inputs(w, workers=workers)      # before any CUDA call (spawn pool)
+    want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
+    cpu = cpu_baseline(OracleStep(w, budget, inp)) if want_cpu else None
+
+    import torch
+    import sparse_kv_page_gb300 as L
+    from sparse_kv_page_gb300 import build as B
+    B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    L.load_library()
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    q = up(inp.q)
+    kc = up(inp.k_cache)
+    vc = up(inp.v_cache)
+    table = up(inp.page_table)
+    seq = up(inp.seq_pages)
+    del inp.k_cache, inp.v_cache
+    dims = L.make_dims(w.batch, w.num_q_heads, w.num_kv_heads, w.pages, w.num_phys_pages)
+    summ = L.Summaries.empty(w.num_phys_pages, w.num_kv_heads, dev)
+    ids = torch.arange(w.num_phys_pages, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # summary build (off the decode critical path): warm once, time once
+    L.locks_build_summaries(dims, kc, ids, w.num_phys_pages, summ)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    L.locks_build_summaries(dims, kc, ids, w.num_phys_pages, summ)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    build_ms = e0.elapsed_time(e1)
+
+    k_cap = L.locks_k_cap(dims, budget)
+    ws = L.alloc_workspace(dims, budget, dev)
+    scores = torch.empty((w.batch, w.num_q_heads, w.pages), dtype=torch.float32, device=dev)
+    sel = torch.empty((w.batch, w.num_kv_heads, k_cap), dtype=torch.int32, device=dev)
+    nsel = torch.empty((w.batch, w.num_kv_heads), dtype=torch.int32, device=dev)
+    out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.int16, device=dev)
+    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        L.locks_score_pages(dims, q, summ, table, seq, scores, ws)
+        L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert L.locks_get_device_status(ws) == 0, "device status after warm-up"
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        L.locks_score_pages(dims, q, summ, table, seq, scores, ws)
+        evs[i][1].record(stream)
+        L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws)
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    sampler.stop()
+    status = L.locks_get_device_status(ws)
+    step_ms = [a.elapsed_time(c) for a, _, c in evs]
+    score_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    sa_ms = [b.elapsed_time(c) for _, b, c in evs]
+    mean_step_us = reduce_max(statistics.mean(step_ms) * 1000.0, world, dev)
+    mean_score_us = reduce_max(statistics.mean(score_ms) * 1000.0, world, dev)
+    mean_sa_us = reduce_max(statistics.mean(sa_ms) * 1000.0, world, dev)
+
+    # end to end through the public call with host buffers: q in, output out
+    q_host = torch.from_numpy(np.ascontiguousarray(synth.make_queries(w))).pin_memory()
+    out_host = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    n_e2e = min(K, 200)
+    e2e_us = []
+    for i in range(n_e2e + 3):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        q.copy_(q_host, non_blocking=True)
+        L.locks_decode_step(dims, q, kc, vc, summ, table, seq, budget, out, ws, lse=lse)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_us.append((time.perf_counter() - t1) * 1e6)
+    e2e_value = reduce_max(statistics.mean(e2e_us), world, dev)
+
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    summ_bytes, kv_bytes = algorithmic_bytes(w, budget)
+    step_bytes = summ_bytes + kv_bytes
+    score_gbs = summ_bytes / (mean_score_us * 1e-6) / 1e9
+    step_gbs = step_bytes / (mean_step_us * 1e-6) / 1e9
+    traffic = recorded_traffic("score_kernel")
+    clocks = sampler.summary()
+    units = w.batch * w.pages * w.num_kv_heads
+    line = {
+        "metric": METRIC, "value": mean_step_us, "unit": "us", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": mean_step_us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4/int8 codes x f16 MMA, fp32 accumulate; bf16 K/V",
+        "data": "synthetic (seeded page-local low-rank keys, N(0,1) values and queries)",
+        "config": config_of(w, budget),
+        "effective_GBps": step_gbs, "algorithmic_bytes_per_step": step_bytes,
+        "frac_of_measured_hbm": step_gbs / hbm, "frac_of_8TBps": step_gbs / NOMINAL_HBM_GBS,
+        "aggregate_effective_GBps": step_gbs * world,
+        "kernels_us": {"score_pages": mean_score_us, "select_attend": mean_sa_us,
+                       "step_p50": statistics.median(step_ms) * 1000.0},
+        "bytes_vs_dense": (w.batch * w.pages * w.num_kv_heads * PAGE_KV_BYTES) / step_bytes,
+        "roofline": {"kernel": "score_pages (locks_score_pages)", "bound": "hbm", "achieved": score_gbs,
+                     "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+                     "frac": score_gbs / hbm,
+                     "algorithmic_bytes_per_launch": summ_bytes, "units_per_launch": units,
+                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                     "traffic_source": traffic["source"] if traffic else None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "us", "h2d_bytes_per_step": int(q_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * 2),
+                "path": "pinned q -> locks_decode_step -> output to pinned host, synchronised, wall clock"},
+        "clocks": clocks, "gpu_launches": 2 * K, "device_status": status,
+        "timed_wall_s": wall,
+        "build": {"units": units, "ms": build_ms, "pages_per_s": w.batch * w.pages / (build_ms * 1e-3),
+                  "units_per_s": units / (build_ms * 1e-3)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["locks", "reference"], default="locks")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="ctx1m")
+    ap.add_argument("--budget", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_locks(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()
