@@ -228,6 +228,34 @@ LOCKS_API int locks_decode_step(const locks_dims_t* dims, const float* q, const 
                                 int32_t* n_selected, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * locks_decode_step without a workspace (the LOCKS pages have no counterpart
+ * of this call; it exists for callers that cannot allocate device memory).
+ * Serving engines usually reserve nearly all of HBM for their own paged KV
+ * pool at start-up and give plugins no allocator, and cudaMalloc may
+ * synchronise the device in the middle of a decode loop; such callers cannot
+ * supply the workspace of locks_decode_step. Here the scratch (the score
+ * table and the selection) lives in a fixed 36 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. The caller still passes all inputs and outputs (out, and lse which
+ * may be NULL).
+ * - Returns LOCKS_ERR_WORKSPACE_TOO_SMALL when locks_workspace_size(dims,
+ *   budget_tokens) exceeds 36 MiB (for example batch 4 x 32 query heads x
+ *   65536 pages fits; batch 8 at the same sizes does not).
+ * - The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ * - All calls share the one array and it keeps the last call's contents:
+ *   calls that overlap on the GPU (other streams, other threads) race and
+ *   must be serialised by the caller.
+ * - Device-side errors (bounded waits, bad page ids) are recorded in the
+ *   array and cannot be read back by the caller; each call starts cleared.
+ * - Calls no allocator (no cudaMalloc / cudaFree).
+ */
+LOCKS_API int locks_decode_step_noalloc(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                        const uint16_t* v_cache, locks_summaries_t summaries,
+                                        const int32_t* page_table, const int32_t* seq_pages,
+                                        int32_t budget_tokens, uint16_t* out, float* lse, void* stream);
+
+/*
  * Copies the device status word (LOCKS_OK, LOCKS_ERR_TIMEOUT or
  * LOCKS_ERR_BAD_INDEX; the first error recorded wins) at the start of the
  * workspace to *status. Synchronises the stream.
