@@ -181,6 +181,8 @@ def recorded_traffic(kernel: str):
 
 def workload_of(args) -> tuple[synth.Workload, int]:
     w = synth.WORKLOADS[args.workload]
+    if args.pages is not None:
+        w = w.scaled(pages=args.pages, name_suffix=f"-{args.pages}p")
     budget = args.budget if args.budget is not None else max(w.budgets)
     return w, budget
 
@@ -343,13 +345,25 @@ def run_locks(args, rank, world, local):
     lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
-    def step():
+    def score():
         L.locks_score_pages(dims, q, summ, table, seq, scores, ws)
+
+    def select_attend():
         L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws)
 
+    # eager warm-up (first-call set-up), then one CUDA graph per kernel of the step
+    score()
+    select_attend()
+    torch.cuda.synchronize()
+    g_score, g_sa = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_score):
+        score()
+    with torch.cuda.graph(g_sa):
+        select_attend()
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        g_score.replay()
+        g_sa.replay()
     torch.cuda.synchronize()
     assert L.locks_get_device_status(ws) == 0, "device status after warm-up"
 
@@ -368,9 +382,9 @@ def run_locks(args, rank, world, local):
     for i in range(K):
         flush.zero_()
         evs[i][0].record(stream)
-        L.locks_score_pages(dims, q, summ, table, seq, scores, ws)
+        g_score.replay()
         evs[i][1].record(stream)
-        L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws)
+        g_sa.replay()
         evs[i][2].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
@@ -435,6 +449,7 @@ def run_locks(args, rank, world, local):
         "e2e": {"value": e2e_value, "unit": "us", "h2d_bytes_per_step": int(q_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host.numel() * 2),
                 "path": "pinned q -> locks_decode_step -> output to pinned host, synchronised, wall clock"},
+        "launch": "one CUDA graph per kernel (score_pages, select_attend), replayed each step",
         "clocks": clocks, "gpu_launches": 2 * K, "device_status": status,
         "timed_wall_s": wall,
         "build": {"units": units, "ms": build_ms, "pages_per_s": w.batch * w.pages / (build_ms * 1e-3),
@@ -451,6 +466,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["locks", "reference"], default="locks")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="ctx1m")
     ap.add_argument("--budget", type=int, default=None)
+    ap.add_argument("--pages", type=int, default=None, help="override pages per sequence (smaller cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -475,7 +475,7 @@ cudaError_t launch_build(const BuildArgs& a, int num_sms, cudaStream_t stream) {
     const int64_t n_units = static_cast<int64_t>(a.n_pages) * a.hkv;
     if (n_units == 0) return cudaSuccess;
     const size_t smem = kWarps * sizeof(WarpSmem);
-    cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_kernel_attrs<build_kernel>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t pairs = (n_units + 1) / 2;
     int64_t grid = (pairs + kWarps - 1) / kWarps;

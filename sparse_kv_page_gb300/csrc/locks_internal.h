@@ -5,9 +5,33 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "locks_common.cuh"
 
 namespace locks {
+
+// Raises a kernel's dynamic shared-memory limit (and allows 16-CTA clusters
+// when asked) once per device instead of on every launch.
+template <auto Kern>
+cudaError_t ensure_kernel_attrs(int smem_bytes, bool nonportable_cluster = false) {
+    static std::atomic<int> done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire) >= smem_bytes + 1) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (nonportable_cluster) {
+        e = cudaFuncSetAttribute(Kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    int prev = done[dev].load();
+    while (prev < smem_bytes + 1 && !done[dev].compare_exchange_weak(prev, smem_bytes + 1)) {
+    }
+    return cudaSuccess;
+}
 
 struct ScoreArgs {
     const float* q;

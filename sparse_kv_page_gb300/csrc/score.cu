@@ -276,11 +276,10 @@ cudaError_t launch_t(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
     const int nchunks = (a.max_pages + NP - 1) / NP;
     const int total = a.batch * nchunks;
     if (total == 0) return cudaSuccess;
-    auto kern = score_kernel<HKV, NT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = ensure_kernel_attrs<score_kernel<HKV, NT>>(kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = min(total, num_sms);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(a, nchunks, total);
+    score_kernel<HKV, NT><<<grid, kThreads, kSmemBytes, stream>>>(a, nchunks, total);
     return cudaGetLastError();
 }
 

@@ -508,12 +508,8 @@ cudaError_t launch_t(const SelectAttendArgs& a, cudaStream_t stream) {
     const int chunk = chunk_of(a.max_pages, CL);
     const size_t smem = select_attend_smem_bytes(a.max_pages, CL, MODE);
     auto kern = select_attend_kernel<CL, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_kernel_attrs<select_attend_kernel<CL, MODE>>(static_cast<int>(smem), CL > 8);
     if (e != cudaSuccess) return e;
-    if (CL > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, a.batch * a.hkv, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -543,10 +539,7 @@ cudaError_t launch_cl(const SelectAttendArgs& a, SAMode mode, cudaStream_t strea
 template <int CL, SAMode MODE>
 int max_active_clusters(size_t smem) {
     auto kern = select_attend_kernel<CL, MODE>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-        return 0;
-    if (CL > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return 0;
+    if (ensure_kernel_attrs<select_attend_kernel<CL, MODE>>(static_cast<int>(smem), CL > 8) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
