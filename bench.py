@@ -343,13 +343,16 @@ def run_locks(args, rank, world, local):
     nsel = torch.empty((w.batch, w.num_kv_heads), dtype=torch.int32, device=dev)
     out = torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.int16, device=dev)
     lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    partials = torch.empty(L.locks.lse_partials_shape(dims), dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
+    # the two kernels locks_decode_step launches (scores + LSE partials, then selection + attention)
     def score():
-        L.locks_score_pages(dims, q, summ, table, seq, scores, ws)
+        L.locks_score_pages(dims, q, summ, table, seq, scores, ws, lse_partials=partials)
 
     def select_attend():
-        L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws)
+        L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws,
+                              lse_partials=partials)
 
     # eager warm-up (first-call set-up), then one CUDA graph per kernel of the step
     score()

@@ -44,6 +44,9 @@
  *   seq_pages         int32 [batch]: full (summarised) pages of each sequence,
  *                     0 <= seq_pages[b] <= max_pages_per_seq
  *   scores            fp32 [batch][num_q_heads][max_pages_per_seq]
+ *   lse_partials      fp32 pairs [batch][num_q_heads][ceil(max_pages_per_seq/8)][2]:
+ *                     (max, sum exp(score - max)) over each 8-page block of a
+ *                     sequence (pages < seq_pages only); optional
  *   selected          int32 [batch][num_kv_heads][k_cap], ascending logical
  *                     page ids, k_cap = locks_k_cap(dims, budget_tokens)
  *   n_selected        int32 [batch][num_kv_heads]
@@ -133,8 +136,8 @@ LOCKS_API int locks_k_cap(const locks_dims_t* dims, int32_t budget_tokens, int32
 
 /*
  * Workspace bytes needed by every call below for these dims and budget
- * (the decode step needs the most: the score table, the selection and the
- * device status word). The workspace must be 256-byte aligned. Its first 256
+ * (the decode step needs the most: the score table, its LSE partials, the
+ * selection and the device status word). The workspace must be 256-byte aligned. Its first 256
  * bytes hold the status word; locks_clear_device_status zeroes it.
  */
 LOCKS_API int locks_workspace_size(const locks_dims_t* dims, int32_t budget_tokens, size_t* bytes);
@@ -163,11 +166,14 @@ LOCKS_API int locks_build_summaries(const locks_dims_t* dims, const uint16_t* k_
  *   scores[b][h][j] = log sum_{i < 16} exp[(q.mu_j + (V_j^T q).c_i) / sqrt(128)]
  * for every sequence b, query head h and logical page j < seq_pages[b], with
  * the summary of unit (page_table[b][j], h / g) dequantised. Entries
- * j >= seq_pages[b] are not written.
+ * j >= seq_pages[b] are not written. When lse_partials is not NULL it also
+ * receives each 8-page block's (max, sum exp) of the scores (layout above),
+ * which the selection uses to form the per-head normaliser without
+ * re-reading the whole score table.
  */
 LOCKS_API int locks_score_pages(const locks_dims_t* dims, const float* q, locks_summaries_t summaries,
                                 const int32_t* page_table, const int32_t* seq_pages, float* scores,
-                                void* workspace, size_t workspace_bytes, void* stream);
+                                float* lse_partials, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Group-shared top-k selection ([summary] 2.3: mean of the estimated mass
@@ -179,11 +185,14 @@ LOCKS_API int locks_score_pages(const locks_dims_t* dims, const float* q, locks_
  * select on the order-preserving 32-bit image of key), equal keys ranked by
  * lower page id, NaN keys ranked below -inf, written in ascending order;
  * n_selected[b][kvh] = k. sel_keys (fp32 [B][Hkv][max_pages_per_seq], may be
- * NULL) receives key_j for j < seq_pages[b].
+ * NULL) receives key_j for j < seq_pages[b]. lse_partials (may be NULL) are
+ * the partials locks_score_pages wrote for these same scores; when given,
+ * L_h is reduced from them.
  */
-LOCKS_API int locks_select_pages(const locks_dims_t* dims, const float* scores, const int32_t* seq_pages,
-                                 int32_t budget_tokens, int32_t* selected, int32_t* n_selected,
-                                 float* sel_keys, void* workspace, size_t workspace_bytes, void* stream);
+LOCKS_API int locks_select_pages(const locks_dims_t* dims, const float* scores, const float* lse_partials,
+                                 const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected,
+                                 int32_t* n_selected, float* sel_keys, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * Attention over the selected pages only ([post] "Code": scaled dot-product
@@ -209,14 +218,14 @@ LOCKS_API int locks_sparse_attention(const locks_dims_t* dims, const float* q, c
  */
 LOCKS_API int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
                                   const uint16_t* v_cache, const int32_t* page_table, const float* scores,
-                                  const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected,
-                                  int32_t* n_selected, uint16_t* out, float* lse, void* workspace,
-                                  size_t workspace_bytes, void* stream);
+                                  const float* lse_partials, const int32_t* seq_pages, int32_t budget_tokens,
+                                  int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The whole decode step ([summary] 2.4: scoring, selection and sparse
- * attention captured together in CUDA graphs): locks_score_pages, then
- * locks_select_attend.
+ * attention captured together in CUDA graphs): locks_score_pages (with LSE
+ * partials), then locks_select_attend.
  * scores, selected and n_selected may be NULL, in which case they live in the
  * workspace; when given they receive the same values as the separate calls.
  * Two kernel launches; no host synchronisation; graph-capturable.

@@ -34,24 +34,44 @@ int num_sms(int dev) {
     return v;
 }
 
-// Cluster size for the select/attend kernels, cached per (device, mode, smem).
-int cluster_size(int dev, int max_pages, locks::SAMode mode) {
+// Cluster size (16 or 8) for the select/attend kernels. A cluster of CL CTAs
+// handles one (sequence, kv head) segment; when the segments do not all fit
+// at once the launch runs in waves, so the choice minimises
+// waves x (pages per CTA + a fixed per-CTA cost in page units). Residency
+// counts come from the occupancy API, cached per (device, mode, group, pages).
+int cluster_size(int dev, const locks_dims_t* d, locks::SAMode mode) {
     struct Entry {
-        int dev, mode;
-        size_t smem;
-        int cl;
+        int dev, mode, gbound, max_pages;
+        int active16, active8;
     };
     static std::mutex mu;
-    static Entry table[64];
+    static Entry table[128];
     static int n = 0;
-    const size_t smem16 = locks::select_attend_smem_bytes(max_pages, 16, mode);
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n; ++i)
-        if (table[i].dev == dev && table[i].mode == static_cast<int>(mode) && table[i].smem == smem16)
-            return table[i].cl;
-    const int cl = locks::select_attend_cluster_size(max_pages, mode);
-    if (n < 64) table[n++] = {dev, static_cast<int>(mode), smem16, cl};
-    return cl;
+    const int g = d->num_q_heads / d->num_kv_heads;
+    const int gbound = g <= 4 ? 4 : 16;
+    int a16 = -1, a8 = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n; ++i)
+            if (table[i].dev == dev && table[i].mode == static_cast<int>(mode) && table[i].gbound == gbound &&
+                table[i].max_pages == d->max_pages_per_seq) {
+                a16 = table[i].active16;
+                a8 = table[i].active8;
+                break;
+            }
+        if (a16 < 0) {
+            a16 = locks::select_attend_active_clusters(d->max_pages_per_seq, mode, g, 16);
+            a8 = locks::select_attend_active_clusters(d->max_pages_per_seq, mode, g, 8);
+            if (n < 128) table[n++] = {dev, static_cast<int>(mode), gbound, d->max_pages_per_seq, a16, a8};
+        }
+    }
+    const long segs = static_cast<long>(d->batch) * d->num_kv_heads;
+    auto cost = [&](int cl, int active) -> double {
+        if (active <= 0) return 1e30;
+        const long waves = (segs + active - 1) / active;
+        return static_cast<double>(waves) * ((d->max_pages_per_seq + cl - 1) / cl + 2048.0);
+    };
+    return cost(16, a16) <= cost(8, a8) ? 16 : 8;
 }
 
 locks::DeviceStatus status_of(void* ws) {
@@ -83,14 +103,15 @@ int k_cap_of(const locks_dims_t* d, int32_t budget) {
 }
 
 struct WsLayout {
-    size_t status, scores, selected, n_selected, total;
+    size_t status, scores, partials, selected, n_selected, total;
 };
 WsLayout ws_layout(const locks_dims_t* d, int32_t budget) {
     WsLayout w;
     const size_t B = static_cast<size_t>(d->batch);
     w.status = 0;
     w.scores = kAlign;
-    w.selected = w.scores + align_up(B * d->num_q_heads * static_cast<size_t>(d->max_pages_per_seq) * 4);
+    w.partials = w.scores + align_up(B * d->num_q_heads * static_cast<size_t>(d->max_pages_per_seq) * 4);
+    w.selected = w.partials + align_up(B * d->num_q_heads * static_cast<size_t>((d->max_pages_per_seq + 7) / 8) * 8);
     w.n_selected = w.selected + align_up(B * d->num_kv_heads * static_cast<size_t>(k_cap_of(d, budget)) * 4);
     w.total = w.n_selected + align_up(B * d->num_kv_heads * 4);
     return w;
@@ -121,7 +142,7 @@ bool select_fits(int max_pages, locks::SAMode mode) {
 }
 
 int score_impl(const locks_dims_t* dims, const float* q, locks_summaries_t s, const int32_t* page_table,
-               const int32_t* seq_pages, float* scores, void* ws, cudaStream_t stream) {
+               const int32_t* seq_pages, float* scores, float* partials, void* ws, cudaStream_t stream) {
     const int dev = current_device();
     if (dev < 0) return LOCKS_ERR_CUDA;
     locks::ScoreArgs a;
@@ -133,6 +154,7 @@ int score_impl(const locks_dims_t* dims, const float* q, locks_summaries_t s, co
     a.page_table = page_table;
     a.seq_pages = seq_pages;
     a.scores = scores;
+    a.lse_partials = partials;
     a.batch = dims->batch;
     a.hq = dims->num_q_heads;
     a.hkv = dims->num_kv_heads;
@@ -154,13 +176,15 @@ locks::SelectAttendArgs sa_args(const locks_dims_t* dims, void* ws) {
 }
 
 int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                       const int32_t* page_table, const float* scores, const int32_t* seq_pages,
+                       const int32_t* page_table, const float* scores, const float* partials,
+                       const int32_t* seq_pages,
                        int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
                        void* workspace, cudaStream_t st) {
     const int dev = current_device();
     if (dev < 0) return LOCKS_ERR_CUDA;
     locks::SelectAttendArgs a = sa_args(dims, workspace);
     a.scores = scores;
+    a.lse_partials = partials;
     a.seq_pages = seq_pages;
     a.selected = selected;
     a.n_selected = n_selected;
@@ -173,7 +197,7 @@ int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t*
     a.page_table = page_table;
     a.out = out;
     a.lse = lse;
-    const int cl = cluster_size(dev, dims->max_pages_per_seq, locks::SAMode::kSelectAttend);
+    const int cl = cluster_size(dev, dims, locks::SAMode::kSelectAttend);
     return cuda_status(locks::launch_select_attend(a, locks::SAMode::kSelectAttend, cl, st));
 }
 
@@ -242,21 +266,22 @@ int locks_build_summaries(const locks_dims_t* dims, const uint16_t* k_cache, con
 }
 
 int locks_score_pages(const locks_dims_t* dims, const float* q, locks_summaries_t summaries,
-                      const int32_t* page_table, const int32_t* seq_pages, float* scores, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+                      const int32_t* page_table, const int32_t* seq_pages, float* scores, float* lse_partials,
+                      void* workspace, size_t workspace_bytes, void* stream) {
     int v = validate_dims(dims);
     if (v != LOCKS_OK) return v;
     if (dims->batch == 0 || dims->max_pages_per_seq == 0) return LOCKS_OK;
     if (!q || !page_table || !seq_pages || !scores || !aligned(q, 16)) return LOCKS_ERR_INVALID_ARG;
+    if (lse_partials && !aligned(lse_partials, 8)) return LOCKS_ERR_INVALID_ARG;
     if ((v = check_summaries(summaries)) != LOCKS_OK) return v;
     if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
-    return score_impl(dims, q, summaries, page_table, seq_pages, scores, workspace,
+    return score_impl(dims, q, summaries, page_table, seq_pages, scores, lse_partials, workspace,
                       static_cast<cudaStream_t>(stream));
 }
 
-int locks_select_pages(const locks_dims_t* dims, const float* scores, const int32_t* seq_pages,
-                       int32_t budget_tokens, int32_t* selected, int32_t* n_selected, float* sel_keys,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+int locks_select_pages(const locks_dims_t* dims, const float* scores, const float* lse_partials,
+                       const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected, int32_t* n_selected,
+                       float* sel_keys, void* workspace, size_t workspace_bytes, void* stream) {
     int v = validate_dims(dims);
     if (v != LOCKS_OK) return v;
     if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
@@ -268,13 +293,14 @@ int locks_select_pages(const locks_dims_t* dims, const float* scores, const int3
     if (dev < 0) return LOCKS_ERR_CUDA;
     locks::SelectAttendArgs a = sa_args(dims, workspace);
     a.scores = scores;
+    a.lse_partials = lse_partials;
     a.seq_pages = seq_pages;
     a.selected = selected;
     a.n_selected = n_selected;
     a.sel_keys = sel_keys;
     a.budget_pages = budget_tokens / LOCKS_PAGE_SIZE;
     a.k_cap = k_cap_of(dims, budget_tokens);
-    const int cl = cluster_size(dev, dims->max_pages_per_seq, locks::SAMode::kSelect);
+    const int cl = cluster_size(dev, dims, locks::SAMode::kSelect);
     return cuda_status(locks::launch_select_attend(a, locks::SAMode::kSelect, cl, static_cast<cudaStream_t>(stream)));
 }
 
@@ -301,14 +327,14 @@ int locks_sparse_attention(const locks_dims_t* dims, const float* q, const uint1
     a.page_table = page_table;
     a.out = out;
     a.lse = lse;
-    const int cl = cluster_size(dev, dims->max_pages_per_seq, locks::SAMode::kAttend);
+    const int cl = cluster_size(dev, dims, locks::SAMode::kAttend);
     return cuda_status(locks::launch_select_attend(a, locks::SAMode::kAttend, cl, static_cast<cudaStream_t>(stream)));
 }
 
 int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                        const int32_t* page_table, const float* scores, const int32_t* seq_pages,
-                        int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+                        const int32_t* page_table, const float* scores, const float* lse_partials,
+                        const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected, int32_t* n_selected,
+                        uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
     int v = validate_dims(dims);
     if (v != LOCKS_OK) return v;
     if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
@@ -318,8 +344,9 @@ int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t
     if (!aligned(q, 8) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return LOCKS_ERR_INVALID_ARG;
     if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
     if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelectAttend)) return LOCKS_ERR_UNSUPPORTED;
-    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
-                              n_selected, out, lse, workspace, static_cast<cudaStream_t>(stream));
+    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, lse_partials, seq_pages,
+                              budget_tokens, selected, n_selected, out, lse, workspace,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int locks_decode_step(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
@@ -340,13 +367,14 @@ int locks_decode_step(const locks_dims_t* dims, const float* q, const uint16_t* 
     if (!scores) scores = reinterpret_cast<float*>(base + L.scores);
     if (!selected) selected = reinterpret_cast<int32_t*>(base + L.selected);
     if (!n_selected) n_selected = reinterpret_cast<int32_t*>(base + L.n_selected);
+    float* partials = reinterpret_cast<float*>(base + L.partials);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dims->max_pages_per_seq > 0) {
-        v = score_impl(dims, q, summaries, page_table, seq_pages, scores, workspace, st);
+        v = score_impl(dims, q, summaries, page_table, seq_pages, scores, partials, workspace, st);
         if (v != LOCKS_OK) return v;
     }
-    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
-                              n_selected, out, lse, workspace, st);
+    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, partials, seq_pages, budget_tokens,
+                              selected, n_selected, out, lse, workspace, st);
 }
 
 int locks_get_device_status(const void* workspace, int32_t* status, void* stream) {

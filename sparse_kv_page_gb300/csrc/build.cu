@@ -68,14 +68,36 @@ __device__ __forceinline__ void schur(float app, float aqq, float apq, float& c,
 
 template <int R>
 __device__ __forceinline__ void jacobi_round(float (&gr)[16], float (&ur)[16], int i, int base) {
-    float c[8], s[8];
+    // this lane's pair (p, q) of the round: its diagonal entry and a_pq
+    float dmine = 0.f, doff = 0.f;
+    int partner = i;
+    bool is_p = true;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int P = pair_p(R, k), Q = pair_q(R, k);
-        const float app = __shfl_sync(0xffffffffu, gr[P], base + P);
-        const float aqq = __shfl_sync(0xffffffffu, gr[Q], base + Q);
-        const float apq = __shfl_sync(0xffffffffu, gr[Q], base + P);
-        schur(app, aqq, apq, c[k], s[k]);
+        if (i == P) {
+            dmine = gr[P];
+            doff = gr[Q];
+            partner = Q;
+            is_p = true;
+        }
+        if (i == Q) {
+            dmine = gr[Q];
+            doff = gr[P];
+            partner = P;
+            is_p = false;
+        }
+    }
+    const float dother = __shfl_sync(0xffffffffu, dmine, base + partner);
+    const float apq = __shfl_sync(0xffffffffu, doff, base + (is_p ? i : partner));   // both lanes use row p's
+    float cm, sm;
+    schur(is_p ? dmine : dother, is_p ? dother : dmine, apq, cm, sm);
+    // every lane needs every pair's rotation for the column update
+    float c[8], s[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        c[k] = __shfl_sync(0xffffffffu, cm, base + pair_p(R, k));
+        s[k] = __shfl_sync(0xffffffffu, sm, base + pair_p(R, k));
     }
     // G <- G J and U <- U J (columns p, q of this lane's rows)
 #pragma unroll
@@ -89,25 +111,6 @@ __device__ __forceinline__ void jacobi_round(float (&gr)[16], float (&ur)[16], i
         ur[Q] = s[k] * up + c[k] * uq;
     }
     // G <- J^T G (rows p, q): combine with the partner row
-    float cm = 1.f, sm = 0.f;
-    int partner = i;
-    bool is_p = true;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int P = pair_p(R, k), Q = pair_q(R, k);
-        if (i == P) {
-            cm = c[k];
-            sm = s[k];
-            partner = Q;
-            is_p = true;
-        }
-        if (i == Q) {
-            cm = c[k];
-            sm = s[k];
-            partner = P;
-            is_p = false;
-        }
-    }
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         const float other = __shfl_sync(0xffffffffu, gr[m], base + partner);
@@ -259,7 +262,7 @@ __device__ void jacobi_top8(WarpSmem& w, int lane) {
         off2 -= dg * dg;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) off2 += __shfl_xor_sync(0xffffffffu, off2, o);
-        const bool done = off2 <= 1e-13f * fro2;
+        const bool done = off2 <= 1e-10f * fro2;   // off-diagonal <= 1e-5 ||G||: below int4 resolution
         if (__all_sync(0xffffffffu, done)) break;
         Rounds<0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14>::run(gr, ur, i, base);
     }

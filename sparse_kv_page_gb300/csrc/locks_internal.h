@@ -42,6 +42,7 @@ struct ScoreArgs {
     const int32_t* page_table;
     const int32_t* seq_pages;
     float* scores;
+    float* lse_partials;      // nullable: (max, sum exp) per (b, q head, 8-page block)
     int batch, hq, hkv, max_pages, num_phys;
     DeviceStatus st;
 };
@@ -50,6 +51,7 @@ cudaError_t launch_score(const ScoreArgs& a, int num_sms, cudaStream_t stream);
 struct SelectAttendArgs {
     // selection
     const float* scores;
+    const float* lse_partials;   // nullable
     const int32_t* seq_pages;
     int32_t* selected;        // [B][Hkv][k_cap]
     int32_t* n_selected;      // [B][Hkv]
@@ -68,8 +70,9 @@ struct SelectAttendArgs {
 };
 enum class SAMode { kSelect, kAttend, kSelectAttend };
 cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream);
-// Largest cluster size (16 or 8) the select/attend kernels can be launched with.
-int select_attend_cluster_size(int max_pages, SAMode mode);
+// Clusters of `cluster` CTAs (8 or 16) of the select/attend kernel that can be
+// resident at once on the current device (0 if it cannot launch).
+int select_attend_active_clusters(int max_pages, SAMode mode, int group, int cluster);
 size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode);
 
 struct BuildArgs {

@@ -11,7 +11,9 @@
 //    64 units per stage (all kv heads of 64/Hkv consecutive logical pages)
 //    into a 4-stage shared-memory ring with bulk async copies (TMA engine,
 //    L2 evict-first) plus 8-byte LDGSTS for the fp16 scales, completion on
-//    mbarriers; 8 consumer warps each own one kv head and 8 pages per stage.
+//    mbarriers; a group of 8 consumer warps takes a stage, each warp one kv
+//    head and 8 pages; two groups work on alternate stages (one group when
+//    the GQA group is > 8, whose register footprint allows only one).
 //  * V^T q and mu . q run on the tensor cores (mma.sync m16n8k16, f16 in,
 //    fp32 accumulate): A = int4/int8 codes (exact in f16), B = the query
 //    split into an f16 high and low part (about 22 significant bits), so the
@@ -27,8 +29,7 @@
 namespace locks {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kGroupWarps = 8;          // consumer warps per stage
 constexpr int kStageUnits = 64;
 constexpr int kStages = 4;
 constexpr int kStMu = 0;
@@ -42,9 +43,18 @@ __device__ __forceinline__ float pow2i(int e) {  // 2^e for |e| <= 126
     return __int_as_float((127 + e) << 23);
 }
 
+template <int NT>
+struct Shape {
+    static constexpr int kGroups = NT <= 2 ? 2 : 1;
+    static constexpr int kConsumerWarps = kGroups * kGroupWarps;
+    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+};
+
 template <int HKV, int NT>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nchunks, int total_items) {
+__global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs a, int nchunks, int total_items) {
     constexpr int NP = kStageUnits / HKV;   // pages per stage
+    constexpr int kGroups = Shape<NT>::kGroups;
+    constexpr int kConsumerWarps = Shape<NT>::kConsumerWarps;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     uint64_t* empty = full + kStages;
@@ -53,7 +63,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nch
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 33);              // 1 expect_tx arrive + 32 LDGSTS arrives
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], kGroupWarps);
         }
         fence_barrier_init();
     }
@@ -66,31 +76,77 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nch
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
+        // Per stage: each lane owns one page of a 32-page window; pages whose
+        // physical ids are consecutive form runs, and the first lane of a run
+        // issues one bulk copy per array for the whole run. The fp16 scales
+        // go by LDGSTS, at most one 16-byte (or 8-byte for Hkv = 1) copy per
+        // lane. The page-table entries of the next stage are loaded before
+        // waiting for a free slot.
         const uint64_t pol = policy_evict_first();
         uint32_t k = 0;
         bool bad = false;
+        int cur_b = -1, cur_P = 0;
+        // page-table prefetch for item `it` (entries of this lane's pages)
+        auto load_phys = [&](int it, int w, int nvalid) -> int64_t {
+            const int b = it / nchunks, page0 = (it % nchunks) * NP;
+            const int pg = w * 32 + lane;
+            return pg < nvalid ? static_cast<int64_t>(a.page_table[static_cast<int64_t>(b) * a.max_pages + page0 + pg])
+                               : int64_t(-1);
+        };
+        constexpr int kWindows = (NP + 31) / 32;
         for (int it = it0; it < it1; ++it) {
             const int b = it / nchunks, page0 = (it % nchunks) * NP;
-            const int nvalid = min(NP, min(a.seq_pages[b], a.max_pages) - page0);
+            if (b != cur_b) {
+                cur_b = b;
+                cur_P = min(a.seq_pages[b], a.max_pages);
+            }
+            const int nvalid = min(NP, cur_P - page0);
             if (nvalid <= 0) continue;
+            int64_t ph[kWindows];
+#pragma unroll
+            for (int w = 0; w < kWindows; ++w) ph[w] = load_phys(it, w, nvalid);
             const int s = k % kStages;
             if (!mbar_wait_bounded(&empty[s], ((k / kStages) & 1) ^ 1, a.st.wait_limit_ns)) failed = true;
             uint8_t* stg = smem + s * kStageBytes;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nvalid * HKV * 768));
             __syncwarp();
-            for (int pg = lane; pg < nvalid; pg += 32) {
-                int64_t phys = a.page_table[static_cast<int64_t>(b) * a.max_pages + page0 + pg];
-                if (phys < 0 || phys >= a.num_phys) {
+#pragma unroll
+            for (int w = 0; w < kWindows; ++w) {
+                const int pg = w * 32 + lane;
+                const int wpages = min(32, nvalid - w * 32);
+                if (wpages <= 0) break;
+                int64_t phys = ph[w];
+                const bool valid = pg < nvalid;
+                if (valid && (phys < 0 || phys >= a.num_phys)) {
                     bad = true;
                     phys = 0;
                 }
-                const int64_t u0 = phys * HKV;
-                bulk_g2s_hint(stg + kStMu + pg * HKV * 128, a.mu + u0 * 128, HKV * 128, &full[s], pol);
-                bulk_g2s_hint(stg + kStBasis + pg * HKV * 512, a.basis + u0 * 512, HKV * 512, &full[s], pol);
-                bulk_g2s_hint(stg + kStCoef + pg * HKV * 128, a.coef + u0 * 128, HKV * 128, &full[s], pol);
-#pragma unroll
-                for (int h = 0; h < HKV; ++h)
-                    cp_async_8(stg + kStScales + (pg * HKV + h) * 8, a.scales + (u0 + h) * 4);
+                const int64_t prev = __shfl_up_sync(0xffffffffu, phys, 1);
+                const bool start = valid && (lane == 0 || phys != prev + 1);
+                const unsigned starts = __ballot_sync(0xffffffffu, start);
+                if (start) {
+                    const unsigned later = starts & ~((2u << lane) - 1u);   // run starts after this lane
+                    const int end = later ? __ffs(later) - 1 : wpages;
+                    const uint32_t n = static_cast<uint32_t>((end - lane) * HKV);
+                    const int64_t u0 = phys * HKV;
+                    bulk_g2s_hint(stg + kStMu + pg * HKV * 128, a.mu + u0 * 128, n * 128, &full[s], pol);
+                    bulk_g2s_hint(stg + kStBasis + pg * HKV * 512, a.basis + u0 * 512, n * 512, &full[s], pol);
+                    bulk_g2s_hint(stg + kStCoef + pg * HKV * 128, a.coef + u0 * 128, n * 128, &full[s], pol);
+                }
+                // scales: HKV even -> 16-byte pieces of two units, else one 8-byte unit per lane
+                constexpr int kUnitsPerCopy = (HKV % 2 == 0) ? 2 : 1;
+                const int pieces = wpages * HKV / kUnitsPerCopy;
+                if (lane < pieces) {
+                    const int unit_in_window = lane * kUnitsPerCopy;
+                    const int wp = unit_in_window / HKV, h = unit_in_window % HKV;
+                    const int64_t pphys = __shfl_sync(__activemask(), phys, wp);
+                    uint8_t* dst = stg + kStScales + ((w * 32 + wp) * HKV + h) * 8;
+                    const uint16_t* src = a.scales + (pphys * HKV + h) * 4;
+                    if (kUnitsPerCopy == 2)
+                        cp_async_16(dst, src);
+                    else
+                        cp_async_8(dst, src);
+                }
             }
             cp_async_arrive_noinc(&full[s]);
             ++k;
@@ -98,18 +154,27 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nch
         if (bad) report_error(a.st, LOCKS_ERR_BAD_INDEX);
     } else {
         // ------------------------------------------------------ consumers
-        const int kvh = warp % HKV, blk = warp / HKV;
+        const int group = warp / kGroupWarps, gw = warp % kGroupWarps;
+        const int kvh = gw % HKV, blk = gw / HKV;
         const int gid = lane >> 2, t = lane & 3;
         const int g = a.hq / HKV;
         uint32_t bq[8][NT][2];
         float qsc[NT];     // 2^e of the output head (4 nt + t) of this thread
-        int cur_b = -1;
+        int cur_b = -1, q_b = -1, cur_P = 0;
         uint32_t k = 0;
         for (int it = it0; it < it1; ++it) {
             const int b = it / nchunks, page0 = (it % nchunks) * NP;
-            const int nvalid = min(NP, min(a.seq_pages[b], a.max_pages) - page0);
-            if (nvalid <= 0) continue;
             if (b != cur_b) {
+                cur_b = b;
+                cur_P = min(a.seq_pages[b], a.max_pages);
+            }
+            const int nvalid = min(NP, cur_P - page0);
+            if (nvalid <= 0) continue;
+            if (static_cast<int>(k % kGroups) != group) {   // the other group's stage
+                ++k;
+                continue;
+            }
+            if (b != q_b) {
                 // Per-head power-of-two pre-scale: max |q'| < 1.
                 int eB[NT], eO[NT];
 #pragma unroll
@@ -155,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nch
                         bq[s][nt][1] = r1;
                     }
                 }
-                cur_b = b;
+                q_b = b;
             }
             const int s = k % kStages;
             if (!mbar_wait_bounded(&full[s], (k / kStages) & 1, a.st.wait_limit_ns)) failed = true;
@@ -235,20 +300,51 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a, int nch
                             const float f = fc * qsc[nt];
                             const float x0 = (d2[0] + d2[1]) * f;
                             const float x1 = (d2[2] + d2[3]) * f;
-                            float m = fmaxf(x0, x1);
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                            float z = fast_exp2(x0 - m) + fast_exp2(x1 - m);
+                            // log2-sum-exp2 over the 16 tokens (8 lanes x 2); the sum is taken
+                            // unshifted and redone with the max factored out only if it leaves
+                            // [2^-100, 2^100] (exact either way up to exp2/log2 rounding)
+                            float z = fast_exp2(x0) + fast_exp2(x1);
                             z += __shfl_xor_sync(0xffffffffu, z, 4);
                             z += __shfl_xor_sync(0xffffffffu, z, 8);
                             z += __shfl_xor_sync(0xffffffffu, z, 16);
+                            float m = 0.f;
+                            if (__any_sync(0xffffffffu, !(z >= 7.9e-31f && z <= 1.26e30f))) {
+                                m = fmaxf(x0, x1);
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                                z = fast_exp2(x0 - m) + fast_exp2(x1 - m);
+                                z += __shfl_xor_sync(0xffffffffu, z, 4);
+                                z += __shfl_xor_sync(0xffffffffu, z, 8);
+                                z += __shfl_xor_sync(0xffffffffu, z, 16);
+                            }
                             const float lse_dev = (m + fast_log2(z)) * kLn2;
                             if (gid == u) {
                                 const float a_term = (accmu[nt][0] + accmu[nt][1]) * smu_row * qsc[nt] * kInvSqrtD;
                                 score_out[nt] = a_term + lse_dev;
                             }
                         }
+                    }
+                }
+                if (a.lse_partials) {
+                    // (max, sum exp) of this warp's 8 pages for each head: one partial per 8-page block
+                    const int nblk = (a.max_pages + 7) / 8;
+                    const int blk8 = (page0 + 8 * blk) / 8;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const float sv = gid < nv ? score_out[nt] : -INFINITY;
+                        float m = sv;
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                        float z = (sv == -INFINITY) ? 0.f : fast_exp2((sv - m) * kLog2e);
+                        z += __shfl_xor_sync(0xffffffffu, z, 4);
+                        z += __shfl_xor_sync(0xffffffffu, z, 8);
+                        z += __shfl_xor_sync(0xffffffffu, z, 16);
+                        const int hh = 4 * nt + t;
+                        if (gid == 0 && hh < g)
+                            reinterpret_cast<float2*>(a.lse_partials)
+                                [(static_cast<int64_t>(b) * a.hq + kvh * g + hh) * nblk + blk8] = make_float2(m, z);
                     }
                 }
                 if (gid < nv) {
@@ -279,7 +375,7 @@ cudaError_t launch_t(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
     cudaError_t e = ensure_kernel_attrs<score_kernel<HKV, NT>>(kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = min(total, num_sms);
-    score_kernel<HKV, NT><<<grid, kThreads, kSmemBytes, stream>>>(a, nchunks, total);
+    score_kernel<HKV, NT><<<grid, Shape<NT>::kThreads, kSmemBytes, stream>>>(a, nchunks, total);
     return cudaGetLastError();
 }
 

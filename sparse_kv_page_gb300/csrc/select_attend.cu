@@ -19,6 +19,10 @@
 // into padded shared rows) and runs QK^T and PV on the tensor cores
 // (mma.sync bf16, query split hi/lo, online softmax in fp32). Warp partials
 // (m, l, o) are merged per CTA, then across the cluster.
+//
+// When the scoring kernel's per-8-page LSE partials are given, the per-head
+// normaliser L_h is reduced from them instead of from the full score table.
+// At most 128 registers per thread so that two CTAs share an SM.
 #include "locks_internal.h"
 
 namespace locks {
@@ -31,8 +35,10 @@ constexpr int kPageSlotBytes = 2 * kPage * kRowBytes; // K rows then V rows: 870
 constexpr int kRingBytes = kWarps * kPageSlotBytes;   // 69,632 B
 constexpr int kPartStride = 2 + kD;                   // m, l, o[128]
 constexpr int kMaxG = LOCKS_MAX_GROUP;
+constexpr int kQRow = 136;                            // bf16 per staged query row (128 + 8 pad)
 
 struct SmallShared {
+    uint16_t qs[2][16 * kQRow];           // query rows (group heads), bf16 high / low parts
     uint32_t hist[2][256];
     float part_m[kMaxG], part_l[kMaxG];   // this CTA's per-head LSE partial
     float Lh[kMaxG];
@@ -80,7 +86,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scan, int& total
 
 // ------------------------------------------------------------- selection
 // Writes selected[b][kvh][0..k) and n_selected[b][kvh]; returns k.
-template <int CL>
+template <int CL, int GM>
 __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk,
                             uint32_t* keys, SmallShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -92,23 +98,63 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * a.max_pages;
 
     // 1. per-head log-sum-exp over the sequence's pages
-    float m[kMaxG], l[kMaxG];
+    float m[GM], l[GM];
 #pragma unroll
-    for (int hh = 0; hh < kMaxG; ++hh) {
+    for (int hh = 0; hh < GM; ++hh) {
         m[hh] = -INFINITY;
         l[hh] = 0.f;
     }
-    for (int j = j0 + tid; j < j1; j += kThreads) {
+    constexpr int kBatch = GM <= 4 ? 4 : 1;   // pages per thread whose loads are all issued before use
+    if (a.lse_partials) {
+        // from the scoring kernel's (max, sum) partials of 8-page blocks
+        const int nblk = (a.max_pages + 7) / 8;
+        const int blk0 = j0 / 8, blk1 = nloc > 0 ? (j1 + 7) / 8 : blk0;   // an empty range owns no block
+        const float2* prow = reinterpret_cast<const float2*>(a.lse_partials) +
+                             (static_cast<int64_t>(b) * a.hq + kvh * g) * nblk;
+        for (int ib = blk0 + tid; ib < blk1; ib += kBatch * kThreads) {
+            float2 v[kBatch][GM];
 #pragma unroll
-        for (int hh = 0; hh < kMaxG; ++hh) {
-            if (hh < g) {
-                const float s = srow[static_cast<int64_t>(hh) * a.max_pages + j];
-                lse_combine(m[hh], l[hh], s, 1.f);
+            for (int u = 0; u < kBatch; ++u) {
+                const int blk = ib + u * kThreads;
+#pragma unroll
+                for (int hh = 0; hh < GM; ++hh)
+                    v[u][hh] = (hh < g && blk < blk1) ? prow[static_cast<int64_t>(hh) * nblk + blk]
+                                                      : make_float2(-INFINITY, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+                for (int hh = 0; hh < GM; ++hh)
+                    if (hh < g) lse_combine(m[hh], l[hh], v[u][hh].x, v[u][hh].y);
+        }
+    } else {
+        for (int jb = j0 + tid; jb < j1; jb += kBatch * kThreads) {
+            float v[kBatch][GM];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int j = jb + u * kThreads;
+#pragma unroll
+                for (int hh = 0; hh < GM; ++hh)
+                    v[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : -INFINITY;
+            }
+#pragma unroll
+            for (int hh = 0; hh < GM; ++hh) {
+                if (hh < g) {
+                    float bm = v[0][hh];
+#pragma unroll
+                    for (int u = 1; u < kBatch; ++u) bm = fmaxf(bm, v[u][hh]);
+                    if (bm != -INFINITY) {
+                        float z = 0.f;
+#pragma unroll
+                        for (int u = 0; u < kBatch; ++u) z += fast_exp2((v[u][hh] - bm) * kLog2e);
+                        lse_combine(m[hh], l[hh], bm, z);
+                    }
+                }
             }
         }
     }
 #pragma unroll
-    for (int hh = 0; hh < kMaxG; ++hh) {
+    for (int hh = 0; hh < GM; ++hh) {
         if (hh < g) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -131,38 +177,59 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     }
     cluster_sync_all();
     if (tid < g) {
+        float pm[CL], pl[CL];   // all remote loads in flight before any use
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) {
+            pm[r] = ld_dsmem_f32(dsmem_addr(&sh.part_m[tid], r));
+            pl[r] = ld_dsmem_f32(dsmem_addr(&sh.part_l[tid], r));
+        }
         float mm = -INFINITY, ll = 0.f;
-        for (uint32_t r = 0; r < CL; ++r)
-            lse_combine(mm, ll, ld_dsmem_f32(dsmem_addr(&sh.part_m[tid], r)),
-                        ld_dsmem_f32(dsmem_addr(&sh.part_l[tid], r)));
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) lse_combine(mm, ll, pm[r], pl[r]);
         sh.Lh[tid] = (ll > 0.f) ? mm + logf(ll) : -INFINITY;
     }
     __syncthreads();
 
     // 2. group-mean mass-share keys
+    // (log2 domain: x = (s - L_h) log2 e; key = (max + log2 sum exp2(x - max)) ln 2 - ln g)
     const float log_g = logf(static_cast<float>(g));
-    for (int j = j0 + tid; j < j1; j += kThreads) {
-        float x[kMaxG];
-        float mx = -INFINITY;
+    float Lr[GM];
 #pragma unroll
-        for (int hh = 0; hh < kMaxG; ++hh) {
-            if (hh < g) {
-                x[hh] = srow[static_cast<int64_t>(hh) * a.max_pages + j] - sh.Lh[hh];
-                mx = fmaxf(mx, x[hh]);
+    for (int hh = 0; hh < GM; ++hh) Lr[hh] = hh < g ? sh.Lh[hh] : 0.f;
+    for (int jb = j0 + tid; jb < j1; jb += kBatch * kThreads) {
+        float v[kBatch][GM];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = jb + u * kThreads;
+#pragma unroll
+            for (int hh = 0; hh < GM; ++hh)
+                v[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = jb + u * kThreads;
+            if (j >= j1) break;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < GM; ++hh) {
+                if (hh < g) {
+                    v[u][hh] = (v[u][hh] - Lr[hh]) * kLog2e;
+                    mx = fmaxf(mx, v[u][hh]);
+                }
             }
-        }
-        float key;
-        if (mx == -INFINITY) {
-            key = -INFINITY;
-        } else {
-            float z = 0.f;
+            float key;
+            if (mx == -INFINITY) {
+                key = -INFINITY;
+            } else {
+                float z = 0.f;
 #pragma unroll
-            for (int hh = 0; hh < kMaxG; ++hh)
-                if (hh < g) z += expf(x[hh] - mx);
-            key = mx + logf(z) - log_g;
+                for (int hh = 0; hh < GM; ++hh)
+                    if (hh < g) z += fast_exp2(v[u][hh] - mx);
+                key = (mx + fast_log2(z)) * kLn2 - log_g;
+            }
+            keys[j - j0] = orderable_key(key);
+            if (a.sel_keys) a.sel_keys[(static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages + j] = key;
         }
-        keys[j - j0] = orderable_key(key);
-        if (a.sel_keys) a.sel_keys[(static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages + j] = key;
     }
     __syncthreads();
 
@@ -204,8 +271,12 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
         }
         __syncthreads();
         cluster_sync_all();
+        uint32_t hv[CL];
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) hv[r] = ld_dsmem_u32(dsmem_addr(&hist[tid], r));
         int total_d = 0;
-        for (uint32_t r = 0; r < CL; ++r) total_d += static_cast<int>(ld_dsmem_u32(dsmem_addr(&hist[tid], r)));
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) total_d += static_cast<int>(hv[r]);
         // suffix count S[d] = sum_{d' >= d} total[d'] = grand - exclusive prefix(d)
         int grand;
         const int excl = block_exclusive_scan(total_d, sh.scan, grand);
@@ -238,9 +309,18 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     }
     cluster_sync_all();
     int base_gt = 0, base_eq = 0;
-    for (uint32_t r = 0; r < rank; ++r) {
-        base_gt += static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.cnt[0], r)));
-        base_eq += static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.cnt[1], r)));
+    {
+        uint32_t cg[CL], ce[CL];
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) {
+            cg[r] = r < rank ? ld_dsmem_u32(dsmem_addr(&sh.cnt[0], r)) : 0u;
+            ce[r] = r < rank ? ld_dsmem_u32(dsmem_addr(&sh.cnt[1], r)) : 0u;
+        }
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) {
+            base_gt += static_cast<int>(cg[r]);
+            base_eq += static_cast<int>(ce[r]);
+        }
     }
     const int take_cta = max(0, min(remaining - base_eq, cta_eq));
     const int pos0 = base_gt + min(base_eq, remaining);
@@ -262,7 +342,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
 }
 
 // ------------------------------------------------------------- attention
-template <int CL>
+template <int CL, int GM>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
                              const int32_t* sel, bool sel_coherent, uint8_t* ring, SmallShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -272,29 +352,21 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     const int p0 = min(n_sel, static_cast<int>(rank) * per);
     const int p1 = min(n_sel, p0 + per);
 
-    // query fragments (rows = the group's heads, scaled by log2(e)/sqrt(d)), bf16 hi/lo
-    uint32_t qh[8][4], ql[8][4];
+    // query rows of the group (scaled by log2(e)/sqrt(d)) staged in shared memory as bf16
+    // high and low parts; the MMA A fragments are read back with ldmatrix
     {
         const float c = kInvSqrtD * kLog2e;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int row = gid + ((r & 1) ? 8 : 0);
-                const int col = 16 * s + 2 * t + ((r & 2) ? 8 : 0);
-                float x0 = 0.f, x1 = 0.f;
-                if (row < g) {
-                    const float2 v = *reinterpret_cast<const float2*>(
-                        a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + row) * kD + col);
-                    x0 = v.x * c;
-                    x1 = v.y * c;
-                }
-                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                qh[s][r] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-                ql[s][r] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
-            }
+        for (int idx = tid; idx < 16 * kD; idx += kThreads) {
+            const int row = idx / kD, col = idx % kD;
+            const float x = row < g ? a.q[(static_cast<int64_t>(b) * a.hq + kvh * g + row) * kD + col] * c : 0.f;
+            const __nv_bfloat16 h = __float2bfloat16_rn(x);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(h));
+            sh.qs[0][row * kQRow + col] = __bfloat16_as_ushort(h);
+            sh.qs[1][row * kQRow + col] = __bfloat16_as_ushort(lo);
         }
+        __syncthreads();
     }
+    const int qrow = (lane & 7) + ((lane >> 3) & 1) * 8, qcol = (lane >> 4) * 8;
     float o[16][4];
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
@@ -334,15 +406,17 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            uint32_t kb[4];
+            uint32_t kb[4], qh[4], ql[4];
             const int mat = lane >> 3;
             const int token = (mat >> 1) * 8 + (lane & 7);
             const int dim = 16 * s + (mat & 1) * 8;
             ldmatrix_x4(kb, kslot + token * kRowBytes + dim * 2);
-            mma_bf16_16816(sacc[0], qh[s], kb[0], kb[1]);
-            mma_bf16_16816(sacc[0], ql[s], kb[0], kb[1]);
-            mma_bf16_16816(sacc[1], qh[s], kb[2], kb[3]);
-            mma_bf16_16816(sacc[1], ql[s], kb[2], kb[3]);
+            ldmatrix_x4(qh, &sh.qs[0][qrow * kQRow + 16 * s + qcol]);
+            ldmatrix_x4(ql, &sh.qs[1][qrow * kQRow + 16 * s + qcol]);
+            mma_bf16_16816(sacc[0], qh, kb[0], kb[1]);
+            mma_bf16_16816(sacc[0], ql, kb[0], kb[1]);
+            mma_bf16_16816(sacc[1], qh, kb[2], kb[3]);
+            mma_bf16_16816(sacc[1], ql, kb[2], kb[3]);
         }
         // online softmax (log2 domain); rows gid (c0, c1) and gid + 8 (c2, c3)
         float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
@@ -450,16 +524,24 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     for (int hh = static_cast<int>(rank); hh < g; hh += CL) {
         if (tid < kD) {
             const float* c = sh.cpart + hh * kPartStride;
+            float mr[CL], lr[CL], orr[CL];   // all remote loads in flight before any use
+#pragma unroll
+            for (uint32_t r = 0; r < CL; ++r) {
+                mr[r] = ld_dsmem_f32(dsmem_addr(c, r));
+                lr[r] = ld_dsmem_f32(dsmem_addr(c + 1, r));
+                orr[r] = ld_dsmem_f32(dsmem_addr(c + 2 + tid, r));
+            }
             float M = -INFINITY;
-            for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, ld_dsmem_f32(dsmem_addr(c, r)));
+#pragma unroll
+            for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, mr[r]);
             float L = 0.f, acc = 0.f;
             if (M != -INFINITY) {
+#pragma unroll
                 for (uint32_t r = 0; r < CL; ++r) {
-                    const float mr = ld_dsmem_f32(dsmem_addr(c, r));
-                    if (mr == -INFINITY) continue;
-                    const float f = fast_exp2(mr - M);
-                    L += ld_dsmem_f32(dsmem_addr(c + 1, r)) * f;
-                    acc += ld_dsmem_f32(dsmem_addr(c + 2 + tid, r)) * f;
+                    if (mr[r] == -INFINITY) continue;
+                    const float f = fast_exp2(mr[r] - M);
+                    L += lr[r] * f;
+                    acc += orr[r] * f;
                 }
             }
             const int64_t qh_idx = static_cast<int64_t>(b) * a.hq + kvh * g + hh;
@@ -471,8 +553,8 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     cluster_sync_all();   // partials stay readable until every CTA is done
 }
 
-template <int CL, SAMode MODE>
-__global__ void __launch_bounds__(kThreads, 1) select_attend_kernel(SelectAttendArgs a, int chunk) {
+template <int CL, SAMode MODE, int GM>
+__global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(SelectAttendArgs a, int chunk) {
     extern __shared__ __align__(128) uint8_t smem[];
     SmallShared& sh = *reinterpret_cast<SmallShared*>(smem);
     uint8_t* big = smem + ((sizeof(SmallShared) + 127) / 128) * 128;
@@ -484,31 +566,32 @@ __global__ void __launch_bounds__(kThreads, 1) select_attend_kernel(SelectAttend
     __syncthreads();
 
     if constexpr (MODE == SAMode::kSelect) {
-        select_pages<CL>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
+        select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
-        attend_pages<CL>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, false,
+        attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, false,
                          big, sh);
     } else {
-        const int n = select_pages<CL>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
-        __threadfence();
+        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
+        // the selection went to global memory; make it visible to the cluster's CTAs
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
         cluster_sync_all();
-        attend_pages<CL>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, true,
+        attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, true,
                          big, sh);
     }
 }
 
 int chunk_of(int max_pages, int cluster) {
     int c = (max_pages + cluster - 1) / cluster;
-    return (c + 3) & ~3;
+    return (c + 7) & ~7;   // whole 8-page blocks (the LSE partials' granularity)
 }
 
-template <int CL, SAMode MODE>
+template <int CL, SAMode MODE, int GM>
 cudaError_t launch_t(const SelectAttendArgs& a, cudaStream_t stream) {
     const int chunk = chunk_of(a.max_pages, CL);
     const size_t smem = select_attend_smem_bytes(a.max_pages, CL, MODE);
-    auto kern = select_attend_kernel<CL, MODE>;
-    cudaError_t e = ensure_kernel_attrs<select_attend_kernel<CL, MODE>>(static_cast<int>(smem), CL > 8);
+    auto kern = select_attend_kernel<CL, MODE, GM>;
+    cudaError_t e = ensure_kernel_attrs<select_attend_kernel<CL, MODE, GM>>(static_cast<int>(smem), CL > 8);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, a.batch * a.hkv, 1);
@@ -527,19 +610,20 @@ cudaError_t launch_t(const SelectAttendArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int CL>
+template <int CL, int GM>
 cudaError_t launch_cl(const SelectAttendArgs& a, SAMode mode, cudaStream_t stream) {
     switch (mode) {
-        case SAMode::kSelect: return launch_t<CL, SAMode::kSelect>(a, stream);
-        case SAMode::kAttend: return launch_t<CL, SAMode::kAttend>(a, stream);
-        default: return launch_t<CL, SAMode::kSelectAttend>(a, stream);
+        case SAMode::kSelect: return launch_t<CL, SAMode::kSelect, GM>(a, stream);
+        case SAMode::kAttend: return launch_t<CL, SAMode::kAttend, GM>(a, stream);
+        default: return launch_t<CL, SAMode::kSelectAttend, GM>(a, stream);
     }
 }
 
-template <int CL, SAMode MODE>
-int max_active_clusters(size_t smem) {
-    auto kern = select_attend_kernel<CL, MODE>;
-    if (ensure_kernel_attrs<select_attend_kernel<CL, MODE>>(static_cast<int>(smem), CL > 8) != cudaSuccess) return 0;
+template <int CL, SAMode MODE, int GM>
+int active_clusters_t(size_t smem) {
+    auto kern = select_attend_kernel<CL, MODE, GM>;
+    if (ensure_kernel_attrs<select_attend_kernel<CL, MODE, GM>>(static_cast<int>(smem), CL > 8) != cudaSuccess)
+        return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -559,6 +643,15 @@ int max_active_clusters(size_t smem) {
     return n;
 }
 
+template <int CL, int GM>
+int active_clusters_cl(size_t smem, SAMode mode) {
+    switch (mode) {
+        case SAMode::kSelect: return active_clusters_t<CL, SAMode::kSelect, GM>(smem);
+        case SAMode::kAttend: return active_clusters_t<CL, SAMode::kAttend, GM>(smem);
+        default: return active_clusters_t<CL, SAMode::kSelectAttend, GM>(smem);
+    }
+}
+
 }  // namespace
 
 size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode) {
@@ -568,22 +661,20 @@ size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode) {
     return small + (keys > ring ? keys : ring);
 }
 
-int select_attend_cluster_size(int max_pages, SAMode mode) {
-    // 16-CTA clusters when the device can co-schedule them, else the portable 8.
-    const size_t smem16 = select_attend_smem_bytes(max_pages, 16, mode);
-    int n16 = 0;
-    switch (mode) {
-        case SAMode::kSelect: n16 = max_active_clusters<16, SAMode::kSelect>(smem16); break;
-        case SAMode::kAttend: n16 = max_active_clusters<16, SAMode::kAttend>(smem16); break;
-        default: n16 = max_active_clusters<16, SAMode::kSelectAttend>(smem16); break;
-    }
-    return n16 > 0 ? 16 : 8;
+int group_bound(int g) { return g <= 4 ? 4 : 16; }
+
+int select_attend_active_clusters(int max_pages, SAMode mode, int g, int cluster) {
+    const size_t smem = select_attend_smem_bytes(max_pages, cluster, mode);
+    if (group_bound(g) == 4)
+        return cluster == 16 ? active_clusters_cl<16, 4>(smem, mode) : active_clusters_cl<8, 4>(smem, mode);
+    return cluster == 16 ? active_clusters_cl<16, 16>(smem, mode) : active_clusters_cl<8, 16>(smem, mode);
 }
 
 cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream) {
     if (a.batch * a.hkv == 0) return cudaSuccess;
-    if (cluster == 16) return launch_cl<16>(a, mode, stream);
-    return launch_cl<8>(a, mode, stream);
+    const int g = a.hq / a.hkv;
+    if (group_bound(g) == 4) return cluster == 16 ? launch_cl<16, 4>(a, mode, stream) : launch_cl<8, 4>(a, mode, stream);
+    return cluster == 16 ? launch_cl<16, 16>(a, mode, stream) : launch_cl<8, 16>(a, mode, stream);
 }
 
 }  // namespace locks

@@ -78,10 +78,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             "locks_k_cap": ([D, I32, ctypes.POINTER(I32)], ctypes.c_int),
             "locks_workspace_size": ([D, I32, ctypes.POINTER(S)], ctypes.c_int),
             "locks_build_summaries": ([D, P, P, I32, SUM, P, S, P], ctypes.c_int),
-            "locks_score_pages": ([D, P, SUM, P, P, P, P, S, P], ctypes.c_int),
-            "locks_select_pages": ([D, P, P, I32, P, P, P, P, S, P], ctypes.c_int),
+            "locks_score_pages": ([D, P, SUM, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_select_pages": ([D, P, P, P, I32, P, P, P, P, S, P], ctypes.c_int),
             "locks_sparse_attention": ([D, P, P, P, P, P, P, I32, P, P, P, S, P], ctypes.c_int),
-            "locks_select_attend": ([D, P, P, P, P, P, P, I32, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_select_attend": ([D, P, P, P, P, P, P, P, I32, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_decode_step": ([D, P, P, P, SUM, P, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_get_device_status": ([P, ctypes.POINTER(I32), P], ctypes.c_int),
             "locks_clear_device_status": ([P, P], ctypes.c_int),
@@ -190,20 +190,25 @@ def locks_build_summaries(dims, k_cache, phys_page_ids, n_pages, summaries: Summ
         _stream(stream)))
 
 
+def lse_partials_shape(dims: locks_dims_t):
+    """Shape of the optional LSE-partials buffer (fp32 pairs per 8-page block)."""
+    return (dims.batch, dims.num_q_heads, (dims.max_pages_per_seq + 7) // 8, 2)
+
+
 def locks_score_pages(dims, q, summaries: Summaries, page_table, seq_pages, scores, workspace=None,
-                      stream=None) -> None:
+                      stream=None, lse_partials=None) -> None:
     ws, nws = _ws(workspace)
     _check("locks_score_pages", load_library().locks_score_pages(
-        ctypes.byref(dims), _ptr(q), summaries.c(), _ptr(page_table), _ptr(seq_pages), _ptr(scores), ws, nws,
-        _stream(stream)))
+        ctypes.byref(dims), _ptr(q), summaries.c(), _ptr(page_table), _ptr(seq_pages), _ptr(scores),
+        _ptr(lse_partials), ws, nws, _stream(stream)))
 
 
 def locks_select_pages(dims, scores, seq_pages, budget_tokens, selected, n_selected, sel_keys=None,
-                       workspace=None, stream=None) -> None:
+                       workspace=None, stream=None, lse_partials=None) -> None:
     ws, nws = _ws(workspace)
     _check("locks_select_pages", load_library().locks_select_pages(
-        ctypes.byref(dims), _ptr(scores), _ptr(seq_pages), int(budget_tokens), _ptr(selected), _ptr(n_selected),
-        _ptr(sel_keys), ws, nws, _stream(stream)))
+        ctypes.byref(dims), _ptr(scores), _ptr(lse_partials), _ptr(seq_pages), int(budget_tokens), _ptr(selected),
+        _ptr(n_selected), _ptr(sel_keys), ws, nws, _stream(stream)))
 
 
 def locks_sparse_attention(dims, q, k_cache, v_cache, page_table, selected, n_selected, k_cap, out, lse=None,
@@ -215,11 +220,12 @@ def locks_sparse_attention(dims, q, k_cache, v_cache, page_table, selected, n_se
 
 
 def locks_select_attend(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
-                        n_selected, out, lse=None, workspace=None, stream=None) -> None:
+                        n_selected, out, lse=None, workspace=None, stream=None, lse_partials=None) -> None:
     ws, nws = _ws(workspace)
     _check("locks_select_attend", load_library().locks_select_attend(
-        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(scores), _ptr(seq_pages),
-        int(budget_tokens), _ptr(selected), _ptr(n_selected), _ptr(out), _ptr(lse), ws, nws, _stream(stream)))
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(scores),
+        _ptr(lse_partials), _ptr(seq_pages), int(budget_tokens), _ptr(selected), _ptr(n_selected), _ptr(out),
+        _ptr(lse), ws, nws, _stream(stream)))
 
 
 def locks_decode_step(dims, q, k_cache, v_cache, summaries: Summaries, page_table, seq_pages, budget_tokens, out,
