@@ -192,6 +192,31 @@ __device__ __forceinline__ void int4x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
     r[2] = hsub2_u32(lop3_and_xor(w8, 0x000f000fu, 0x64086408u), k1032);
     r[3] = hfma2_u32(lop3_and_xor(w8, 0x00f000f0u, 0x64806480u), k1_16, km72);
 }
+// Eight int4 codes (nibbles n0..n7 of w) as f16 subnormals of the offset
+// codes u = x + 8 in [1, 15]: r[0] = (u0, u4) * 2^-24, r[1] = (u1, u5) * 16 * 2^-24,
+// r[2] = (u2, u6) * 2^-24, r[3] = (u3, u7) * 16 * 2^-24. One LOP3 per register
+// (mask, then XOR 8 into the nibble); exact. The factor 16 of r[1], r[3] is
+// cancelled by dividing the matching rows of the other MMA operand by 16, and
+// the offset 8 by subtracting 8 * (sum of that operand) from the product.
+__device__ __forceinline__ void int4x8_to_f16x2_sub(uint32_t w, uint32_t (&r)[4]) {
+    const uint32_t w8 = w >> 8;
+    r[0] = lop3_and_xor(w, 0x000f000fu, 0x00080008u);
+    r[1] = lop3_and_xor(w, 0x00f000f0u, 0x00800080u);
+    r[2] = lop3_and_xor(w8, 0x000f000fu, 0x00080008u);
+    r[3] = lop3_and_xor(w8, 0x00f000f0u, 0x00800080u);
+}
+// Four int8 codes as f16 subnormals of u = x + 128: lo = (u0, u1) * 2^-24,
+// hi = (u2, u3) * 2^-24. Exact; the offset is removed as above.
+__device__ __forceinline__ void int8x4_to_f16x2_sub(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    lo = prmt(x, 0u, 0x4140u);
+    hi = prmt(x, 0u, 0x4342u);
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 // Four int8 codes (bytes b0..b3 of w) to f16x2 (b0, b1) and (b2, b3). Exact.
 __device__ __forceinline__ void int8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
     const uint32_t k1152 = 0x64806480u;     // (1152, 1152)

@@ -15,11 +15,14 @@
 //    head and 8 pages; two groups work on alternate stages (one group when
 //    the GQA group is > 8, whose register footprint allows only one).
 //  * V^T q and mu . q run on the tensor cores (mma.sync m16n8k16, f16 in,
-//    fp32 accumulate): A = int4/int8 codes (exact in f16), B = the query
-//    split into an f16 high and low part (about 22 significant bits), so the
-//    products match fp32 arithmetic to well below the 1e-3 score tolerance.
-//    The query is pre-scaled by a power of two per head so the f16 parts
-//    never overflow.
+//    fp32 accumulate): A = the codes plus their offset (int4 + 8, int8 + 128),
+//    read directly as f16 subnormals u * 2^-24 by masking (no conversion
+//    arithmetic; codes from the upper nibble come out as 16u and meet query
+//    rows pre-divided by 16); B = the query split into an f16 high and low
+//    part (about 22 significant bits), so the products match fp32 arithmetic
+//    to well below the 1e-3 score tolerance. The offset is taken out with the
+//    per-head sum of the query, and the query is pre-scaled by a power of two
+//    per head so the f16 parts never overflow.
 //  * the per-token reconstruction (V^T q) . c_i is a second MMA (m16n8k8)
 //    whose B operand is the first MMA's accumulator, split hi/lo and
 //    transposed in registers with movmatrix; the page LSE is a 3-step
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
         const int gid = lane >> 2, t = lane & 3;
         const int g = a.hq / HKV;
         uint32_t bq[8][NT][2];
+        float qsum[NT];    // sum of that head's pre-scaled query q' (code-offset correction)
         float qsc[NT];     // 2^e of the output head (4 nt + t) of this thread
         int cur_b = -1, q_b = -1, cur_P = 0;
         uint32_t k = 0;
@@ -178,24 +182,34 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                 // Per-head power-of-two pre-scale: max |q'| < 1.
                 int eB[NT], eO[NT];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) eB[nt] = eO[nt] = 0;
+                for (int nt = 0; nt < NT; ++nt) {
+                    eB[nt] = eO[nt] = 0;
+                    qsum[nt] = 0.f;
+                }
 #pragma unroll
                 for (int hh = 0; hh < 4 * NT; ++hh) {
-                    float mx = 0.f;
+                    float mx = 0.f, sm = 0.f;
                     if (hh < g) {
                         const float4 v = *reinterpret_cast<const float4*>(
                             a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * kD + lane * 4);
                         mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                        sm = (v.x + v.y) + (v.z + v.w);
                     }
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    for (int o = 16; o > 0; o >>= 1) {
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        sm += __shfl_xor_sync(0xffffffffu, sm, o);
+                    }
                     int e = 0;
                     if (mx > 0.f && mx < INFINITY) e = ilogbf(mx) + 1;
                     e = max(-100, min(100, e));
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         if (((nt * 8 + gid) >> 1) == hh) eB[nt] = e;
-                        if (4 * nt + t == hh) eO[nt] = e;
+                        if (4 * nt + t == hh) {
+                            eO[nt] = e;
+                            qsum[nt] = sm * pow2i(-e);
+                        }
                     }
                 }
 #pragma unroll
@@ -211,7 +225,9 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                             const float2 x01 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t);
                             const float2 x89 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t + 8);
                             const uint32_t p0 = split_f16_hilo(x01.x * inv), p1 = split_f16_hilo(x01.y * inv);
-                            const uint32_t p8 = split_f16_hilo(x89.x * inv), p9 = split_f16_hilo(x89.y * inv);
+                            // rows d + 8, d + 9 divided by 16: they meet the 16x-scaled codes
+                            const uint32_t p8 = split_f16_hilo(x89.x * inv * 0.0625f),
+                                           p9 = split_f16_hilo(x89.y * inv * 0.0625f);
                             // hl = 0: high parts (low halves), hl = 1: low parts (high halves)
                             r0 = hl ? __byte_perm(p0, p1, 0x7632) : __byte_perm(p0, p1, 0x5410);
                             r1 = hl ? __byte_perm(p8, p9, 0x7632) : __byte_perm(p8, p9, 0x5410);
@@ -248,10 +264,12 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         uint32_t lo, hi;
-                        int8x4_to_f16x2(mw[ks], lo, hi);
+                        int8x4_to_f16x2_sub(mw[ks], lo, hi);
                         const uint32_t af[4] = {lo, 0u, hi, 0u};
+                        // B rows d + 8, d + 9 back to full size (x16) for the int8 codes
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(accmu[nt], af, bq[ks][nt][0], bq[ks][nt][1]);
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_f16_16816(accmu[nt], af, bq[ks][nt][0], hmul2_u32(bq[ks][nt][1], 0x4c004c00u));
                     }
                 }
                 const float smu_row = __shfl_sync(0xffffffffu, s_mu, gid);
@@ -272,8 +290,8 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t ra[4], rb[4];
-                        int4x8_to_f16x2(wa[j], ra);
-                        int4x8_to_f16x2(wb[j], rb);
+                        int4x8_to_f16x2_sub(wa[j], ra);
+                        int4x8_to_f16x2_sub(wb[j], rb);
                         const uint32_t a0[4] = {ra[0], rb[0], ra[1], rb[1]};   // k-step 2j
                         const uint32_t a1[4] = {ra[2], rb[2], ra[3], rb[3]};   // k-step 2j + 1
 #pragma unroll
@@ -293,7 +311,9 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                         int8x4_to_f16x2(cw, ca0, ca1);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const float w = (half == 0 ? acc[nt][0] + acc[nt][1] : acc[nt][2] + acc[nt][3]) * svu;
+                            // W' = s_V (sum_k (x_k + 8) q'_k - 8 sum_k q'_k); the MMA sum carries 2^-24
+                            const float raw = half == 0 ? acc[nt][0] + acc[nt][1] : acc[nt][2] + acc[nt][3];
+                            const float w = fmaf(raw, 16777216.f, -8.f * qsum[nt]) * svu;
                             const uint32_t bw = movmatrix_trans(split_f16_hilo(w));
                             float d2[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_f16_1688(d2, ca0, ca1, bw);
@@ -320,7 +340,8 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                             }
                             const float lse_dev = (m + fast_log2(z)) * kLn2;
                             if (gid == u) {
-                                const float a_term = (accmu[nt][0] + accmu[nt][1]) * smu_row * qsc[nt] * kInvSqrtD;
+                                const float a_raw = fmaf(accmu[nt][0] + accmu[nt][1], 16777216.f, -128.f * qsum[nt]);
+                                const float a_term = a_raw * smu_row * qsc[nt] * kInvSqrtD;
                                 score_out[nt] = a_term + lse_dev;
                             }
                         }
