@@ -282,4 +282,16 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ int4 ld_dsmem_v4(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
 }  // namespace locks

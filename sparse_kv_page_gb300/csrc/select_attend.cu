@@ -43,9 +43,9 @@ struct SmallShared {
     float part_m[kMaxG], part_l[kMaxG];   // this CTA's per-head LSE partial
     float Lh[kMaxG];
     float red_m[kWarps][kMaxG], red_l[kWarps][kMaxG];
-    int scan[kWarps + 1];
-    int cnt[2];                           // this CTA's (greater, equal) counts
-    int digit, above;
+    uint32_t tot[3][256];                 // radix pass: bin counts of all CTAs, lower-ranked CTAs, this CTA
+    int wcnt[kWarps][2];
+    int digit, above, above_low, above_own, eq_low, eq_own;
     uint64_t bar[kWarps];
     float cpart[kMaxG * kPartStride];     // this CTA's attention partial per head
 };
@@ -57,123 +57,115 @@ __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float 
     m = M;
 }
 
-// Block-wide exclusive scan of one int per thread; returns (exclusive, total).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scan, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) scan[warp] = x;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            const int c = scan[w];
-            scan[w] = acc;
-            acc += c;
-        }
-        scan[kWarps] = acc;
-    }
-    __syncthreads();
-    const int excl = scan[warp] + x - v;
-    total = scan[kWarps];
-    __syncthreads();
-    return excl;
-}
-
 // ------------------------------------------------------------- selection
-// Writes selected[b][kvh][0..k) and n_selected[b][kvh]; returns k.
+// Per-head normaliser L_h over the sequence (cluster-wide) and the group keys of
+// this CTA's pages [j0, j1) into keys[] (order-preserving uint32 images).
+// Scores are read in batches of kB pages per thread, each batch's loads issued
+// one batch ahead (the first one before the normaliser's reduction, so its
+// latency overlaps the cluster exchange). Loops stay rolled: this code runs
+// about once per launch, and its instruction fetch is what it waits on.
 template <int CL, int GM>
-__device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk,
-                            uint32_t* keys, SmallShared& sh) {
+__device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, uint32_t* keys,
+                           SmallShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = a.hq / a.hkv;
-    const int P = max(0, min(a.seq_pages[b], a.max_pages));
-    const int j0 = min(P, static_cast<int>(rank) * chunk);
-    const int j1 = min(P, j0 + chunk);
     const int nloc = j1 - j0;
     const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * a.max_pages;
+    constexpr int kB = GM <= 4 ? 4 : 1;   // pages per thread per batch
+    constexpr int kStep = kB * kThreads;
+    auto load_batch = [&](float (&x)[kB][GM], int jb) {
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int j = jb + u * kThreads;
+#pragma unroll
+            for (int hh = 0; hh < GM; ++hh)
+                x[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : -INFINITY;
+        }
+    };
+    float v[kB][GM];
+    load_batch(v, j0 + tid);
 
-    // 1. per-head log-sum-exp over the sequence's pages
+    // 1. per-head log-sum-exp over the sequence's pages: (m, l) per thread and head
     float m[GM], l[GM];
 #pragma unroll
     for (int hh = 0; hh < GM; ++hh) {
         m[hh] = -INFINITY;
         l[hh] = 0.f;
     }
-    constexpr int kBatch = GM <= 4 ? 4 : 1;   // pages per thread whose loads are all issued before use
     if (a.lse_partials) {
         // from the scoring kernel's (max, sum) partials of 8-page blocks
         const int nblk = (a.max_pages + 7) / 8;
         const int blk0 = j0 / 8, blk1 = nloc > 0 ? (j1 + 7) / 8 : blk0;   // an empty range owns no block
         const float2* prow = reinterpret_cast<const float2*>(a.lse_partials) +
                              (static_cast<int64_t>(b) * a.hq + kvh * g) * nblk;
-        for (int ib = blk0 + tid; ib < blk1; ib += kBatch * kThreads) {
-            float2 v[kBatch][GM];
+#pragma unroll 1
+        for (int ib = blk0 + tid; ib < blk1; ib += kThreads) {
+            float2 pv[GM];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int blk = ib + u * kThreads;
+            for (int hh = 0; hh < GM; ++hh)
+                pv[hh] = hh < g ? prow[static_cast<int64_t>(hh) * nblk + ib] : make_float2(-INFINITY, 0.f);
 #pragma unroll
-                for (int hh = 0; hh < GM; ++hh)
-                    v[u][hh] = (hh < g && blk < blk1) ? prow[static_cast<int64_t>(hh) * nblk + blk]
-                                                      : make_float2(-INFINITY, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-#pragma unroll
-                for (int hh = 0; hh < GM; ++hh)
-                    if (hh < g) lse_combine(m[hh], l[hh], v[u][hh].x, v[u][hh].y);
+            for (int hh = 0; hh < GM; ++hh)
+                if (hh < g) lse_combine(m[hh], l[hh], pv[hh].x, pv[hh].y);
         }
     } else {
-        for (int jb = j0 + tid; jb < j1; jb += kBatch * kThreads) {
-            float v[kBatch][GM];
+        // from the scores themselves (reloading them later if they span several batches)
+#pragma unroll 1
+        for (int jb = j0 + tid; jb < j1; jb += kStep) {
+            float x[kB][GM];
+            if (jb == j0 + tid) {
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int j = jb + u * kThreads;
+                for (int u = 0; u < kB; ++u)
 #pragma unroll
-                for (int hh = 0; hh < GM; ++hh)
-                    v[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : -INFINITY;
+                    for (int hh = 0; hh < GM; ++hh) x[u][hh] = v[u][hh];
+            } else {
+                load_batch(x, jb);
             }
 #pragma unroll
             for (int hh = 0; hh < GM; ++hh) {
                 if (hh < g) {
-                    float bm = v[0][hh];
+                    float bm = x[0][hh];
 #pragma unroll
-                    for (int u = 1; u < kBatch; ++u) bm = fmaxf(bm, v[u][hh]);
+                    for (int u = 1; u < kB; ++u) bm = fmaxf(bm, x[u][hh]);
                     if (bm != -INFINITY) {
                         float z = 0.f;
 #pragma unroll
-                        for (int u = 0; u < kBatch; ++u) z += fast_exp2((v[u][hh] - bm) * kLog2e);
+                        for (int u = 0; u < kB; ++u) z += fast_exp2((x[u][hh] - bm) * kLog2e);
                         lse_combine(m[hh], l[hh], bm, z);
                     }
                 }
             }
         }
     }
+    // warp reduction: max first, then the sums rescaled to it
 #pragma unroll
     for (int hh = 0; hh < GM; ++hh) {
         if (hh < g) {
+            float M = m[hh];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m[hh], o);
-                const float l2 = __shfl_xor_sync(0xffffffffu, l[hh], o);
-                lse_combine(m[hh], l[hh], m2, l2);
-            }
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float z = (m[hh] == -INFINITY) ? 0.f : l[hh] * fast_exp2((m[hh] - M) * kLog2e);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
             if (lane == 0) {
-                sh.red_m[warp][hh] = m[hh];
-                sh.red_l[warp][hh] = l[hh];
+                sh.red_m[warp][hh] = M;
+                sh.red_l[warp][hh] = z;
             }
         }
     }
     __syncthreads();
     if (tid < g) {
-        float mm = -INFINITY, ll = 0.f;
-        for (int w = 0; w < kWarps; ++w) lse_combine(mm, ll, sh.red_m[w][tid], sh.red_l[w][tid]);
-        sh.part_m[tid] = mm;
-        sh.part_l[tid] = ll;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sh.red_m[w][tid]);
+        float z = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)
+                if (sh.red_m[w][tid] != -INFINITY) z += sh.red_l[w][tid] * fast_exp2((sh.red_m[w][tid] - M) * kLog2e);
+        }
+        sh.part_m[tid] = M;
+        sh.part_l[tid] = z;
     }
     cluster_sync_all();
     if (tid < g) {
@@ -183,10 +175,16 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
             pm[r] = ld_dsmem_f32(dsmem_addr(&sh.part_m[tid], r));
             pl[r] = ld_dsmem_f32(dsmem_addr(&sh.part_l[tid], r));
         }
-        float mm = -INFINITY, ll = 0.f;
+        float M = -INFINITY;
 #pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) lse_combine(mm, ll, pm[r], pl[r]);
-        sh.Lh[tid] = (ll > 0.f) ? mm + logf(ll) : -INFINITY;
+        for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, pm[r]);
+        float z = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (uint32_t r = 0; r < CL; ++r)
+                if (pm[r] != -INFINITY) z += pl[r] * fast_exp2((pm[r] - M) * kLog2e);
+        }
+        sh.Lh[tid] = (z > 0.f) ? M + logf(z) : -INFINITY;
     }
     __syncthreads();
 
@@ -196,151 +194,238 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     float Lr[GM];
 #pragma unroll
     for (int hh = 0; hh < GM; ++hh) Lr[hh] = hh < g ? sh.Lh[hh] : 0.f;
-    for (int jb = j0 + tid; jb < j1; jb += kBatch * kThreads) {
-        float v[kBatch][GM];
+#pragma unroll 1
+    for (int jb = j0 + tid; jb < j1; jb += kStep) {
+        float w[kB][GM];
+        const bool more = jb + kStep < j1;
+        if (more) load_batch(w, jb + kStep);   // next batch in flight while this one is used
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kB; ++u) {
             const int j = jb + u * kThreads;
+            if (j < j1) {
+                float mx = -INFINITY;
+                float x[GM];
 #pragma unroll
-            for (int hh = 0; hh < GM; ++hh)
-                v[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int j = jb + u * kThreads;
-            if (j >= j1) break;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int hh = 0; hh < GM; ++hh) {
-                if (hh < g) {
-                    v[u][hh] = (v[u][hh] - Lr[hh]) * kLog2e;
-                    mx = fmaxf(mx, v[u][hh]);
+                for (int hh = 0; hh < GM; ++hh) {
+                    x[hh] = 0.f;
+                    if (hh < g) {
+                        x[hh] = (v[u][hh] - Lr[hh]) * kLog2e;
+                        mx = fmaxf(mx, x[hh]);
+                    }
                 }
-            }
-            float key;
-            if (mx == -INFINITY) {
-                key = -INFINITY;
-            } else {
-                float z = 0.f;
+                float key;
+                if (mx == -INFINITY) {
+                    key = -INFINITY;
+                } else {
+                    float z = 0.f;
 #pragma unroll
-                for (int hh = 0; hh < GM; ++hh)
-                    if (hh < g) z += fast_exp2(v[u][hh] - mx);
-                key = (mx + fast_log2(z)) * kLn2 - log_g;
+                    for (int hh = 0; hh < GM; ++hh)
+                        if (hh < g) z += fast_exp2(x[hh] - mx);
+                    key = (mx + fast_log2(z)) * kLn2 - log_g;
+                }
+                keys[j - j0] = orderable_key(key);
+                if (a.sel_keys) a.sel_keys[(static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages + j] = key;
             }
-            keys[j - j0] = orderable_key(key);
-            if (a.sel_keys) a.sel_keys[(static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages + j] = key;
+        }
+        if (more) {
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+#pragma unroll
+                for (int hh = 0; hh < GM; ++hh) v[u][hh] = w[u][hh];
         }
     }
     __syncthreads();
+}
+
+// Ordered compaction: visits the keys kept by (T, take_eq) -- every key > T and the
+// first take_eq keys == T in index order -- and calls emit(i, pos) with each kept
+// index and its rank among the kept ones. Each warp walks one contiguous range,
+// four groups of 32 keys per step (conflict-free; ranks from ballots).
+template <typename F>
+__device__ int ordered_keep(const uint32_t* keys, int n, uint32_t T, int take_eq, SmallShared& sh, F emit) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_w = (((n + kWarps - 1) / kWarps) + 127) & ~127;
+    const int w0 = min(n, warp * per_w), w1 = min(n, w0 + per_w);
+    const unsigned lt = lanemask_lt();
+    int ngt = 0, neq = 0;
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+        uint32_t key[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 32 * u + lane;
+            key[u] = i < w1 ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool valid = i0 + 32 * u + lane < w1;
+            ngt += __popc(__ballot_sync(0xffffffffu, valid && key[u] > T));
+            neq += __popc(__ballot_sync(0xffffffffu, valid && key[u] == T));
+        }
+    }
+    if (lane == 0) {
+        sh.wcnt[warp][0] = ngt;
+        sh.wcnt[warp][1] = neq;
+    }
+    __syncthreads();
+    int gt_pre = 0, eq_pre = 0, gt_all = 0, eq_all = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) {
+            gt_pre += sh.wcnt[w][0];
+            eq_pre += sh.wcnt[w][1];
+        }
+        gt_all += sh.wcnt[w][0];
+        eq_all += sh.wcnt[w][1];
+    }
+    int pos = gt_pre + min(eq_pre, take_eq), eq_seen = eq_pre;
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+        uint32_t key[4];
+        unsigned eqb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 32 * u + lane;
+            key[u] = i < w1 ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) eqb[u] = __ballot_sync(0xffffffffu, i0 + 32 * u + lane < w1 && key[u] == T);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 32 * u + lane;
+            const bool eq = (eqb[u] >> lane) & 1u;
+            const bool keep = i < w1 && (key[u] > T || (eq && eq_seen + __popc(eqb[u] & lt) < take_eq));
+            const unsigned kb = __ballot_sync(0xffffffffu, keep);
+            if (keep) emit(i, pos + __popc(kb & lt));
+            pos += __popc(kb);
+            eq_seen += __popc(eqb[u]);
+        }
+    }
+    return gt_all + min(eq_all, take_eq);
+}
+
+// Writes selected[b][kvh][0..K) and n_selected[b][kvh]; returns K.
+// One MSB-first radix select over the cluster (4 passes of 8 bits): each CTA
+// histograms its own keys, every CTA sums the CTAs' histograms through DSMEM and
+// picks the digit. The same pass also yields, per CTA, how many keys lie above
+// the chosen bin in lower-ranked CTAs and in this one (and, in the last pass,
+// how many equal T), which places this CTA's kept keys in the ascending output
+// without a further exchange.
+template <int CL, int GM>
+__device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk, uint32_t* keys,
+                            SmallShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = max(0, min(a.seq_pages[b], a.max_pages));
+    const int j0 = min(P, static_cast<int>(rank) * chunk);
+    const int j1 = min(P, j0 + chunk);
+    const int nloc = j1 - j0;
+
+    group_keys<CL, GM>(a, b, kvh, j0, j1, keys, sh);
 
     int K = min(a.budget_pages, min(P, a.k_cap));
     K = max(K, 0);
     int32_t* out = a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap;
     if (rank == 0 && tid == 0) a.n_selected[b * a.hkv + kvh] = K;
-    if (K == 0) {
-        cluster_sync_all();
-        return 0;
-    }
+    if (K == 0) return 0;
     if (K == P) {
         for (int j = j0 + tid; j < j1; j += kThreads) out[j] = j;
-        cluster_sync_all();
         return K;
     }
 
-    // 3. radix select of the K-th largest key
     uint32_t prefix = 0;
     int remaining = K;
+    int gt_low = 0, gt_own = 0, eq_low = 0, eq_own = 0;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        uint32_t* hist = sh.hist[pass & 1];
-        hist[tid] = 0;
+        uint32_t* hist = sh.hist[pass & 1];   // alternating: other CTAs read the previous one
+        hist[tid] = 0u;
         __syncthreads();
-        // warp-aggregated: one shared atomic per distinct bin per warp step
-        for (int i0 = 0; i0 < nloc; i0 += kThreads) {
-            const int i = i0 + tid;
-            bool take = false;
-            uint32_t bin = 0xffffffffu;
-            if (i < nloc) {
-                const uint32_t key = keys[i];
-                take = pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8));
-                if (take) bin = (key >> shift) & 255u;
+        if (pass == 0) {
+            // the top byte takes few values: one shared atomic per distinct bin per warp step
+            for (int i0 = 0; i0 < nloc; i0 += kThreads) {
+                const int i = i0 + tid;
+                const uint32_t bin = i < nloc ? keys[i] >> 24 : 0xffffffffu;
+                const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                if (i < nloc && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
             }
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (take && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
+        } else {
+            const uint32_t hp = prefix >> (shift + 8);
+#pragma unroll 4
+            for (int i = tid; i < nloc; i += kThreads) {
+                const uint32_t key = keys[i];
+                if ((key >> (shift + 8)) == hp) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
         }
         __syncthreads();
         cluster_sync_all();
-        uint32_t hv[CL];
+        uint32_t hv[CL];   // all remote loads in flight before any use
 #pragma unroll
         for (uint32_t r = 0; r < CL; ++r) hv[r] = ld_dsmem_u32(dsmem_addr(&hist[tid], r));
-        int total_d = 0;
+        uint32_t all = 0u, low = 0u;
 #pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) total_d += static_cast<int>(hv[r]);
-        // suffix count S[d] = sum_{d' >= d} total[d'] = grand - exclusive prefix(d)
-        int grand;
-        const int excl = block_exclusive_scan(total_d, sh.scan, grand);
-        const int S = grand - excl;
-        if (S >= remaining && S - total_d < remaining) {
-            sh.digit = tid;
-            sh.above = S - total_d;
+        for (uint32_t r = 0; r < CL; ++r) {
+            all += hv[r];
+            low += r < rank ? hv[r] : 0u;
+        }
+        sh.tot[0][tid] = all;
+        sh.tot[1][tid] = low;
+        sh.tot[2][tid] = hist[tid];
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds bins 8l .. 8l + 7 of (all CTAs, lower-ranked CTAs, this CTA);
+            // the digit is the bin where the count of keys at or above it first
+            // reaches `remaining`, scanning from the top bin down
+            int c[3][8], t[3], suf[3];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const uint4 h0 = *reinterpret_cast<const uint4*>(&sh.tot[k][8 * lane]);
+                const uint4 h1 = *reinterpret_cast<const uint4*>(&sh.tot[k][8 * lane + 4]);
+                c[k][0] = h0.x; c[k][1] = h0.y; c[k][2] = h0.z; c[k][3] = h0.w;
+                c[k][4] = h1.x; c[k][5] = h1.y; c[k][6] = h1.z; c[k][7] = h1.w;
+                t[k] = ((c[k][0] + c[k][1]) + (c[k][2] + c[k][3])) + ((c[k][4] + c[k][5]) + (c[k][6] + c[k][7]));
+                suf[k] = t[k];
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const int y = __shfl_down_sync(0xffffffffu, suf[k], o);
+                    if (lane + o < 32) suf[k] += y;
+                }
+            }
+            int ab[3];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) ab[k] = suf[k] - t[k];   // keys in the bins of higher lanes
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                if (ab[0] < remaining && ab[0] + c[0][i] >= remaining) {
+                    sh.digit = 8 * lane + i;
+                    sh.above = ab[0];
+                    sh.above_low = ab[1];
+                    sh.above_own = ab[2];
+                    sh.eq_low = c[1][i];
+                    sh.eq_own = c[2][i];
+                }
+#pragma unroll
+                for (int k = 0; k < 3; ++k) ab[k] += c[k][i];
+            }
         }
         __syncthreads();
         prefix |= static_cast<uint32_t>(sh.digit) << shift;
         remaining -= sh.above;
-        __syncthreads();
+        gt_low += sh.above_low;
+        gt_own += sh.above_own;
+        eq_low = sh.eq_low;
+        eq_own = sh.eq_own;
     }
-    const uint32_t T = prefix;   // the K-th largest key; `remaining` keys equal to T are kept
-
-    // 4. ordered compaction: keys > T, then the first `remaining` keys == T
-    const int per_t = (nloc + kThreads - 1) / kThreads;
-    const int i0 = min(nloc, tid * per_t), i1 = min(nloc, i0 + per_t);
-    int ngt = 0, neq = 0;
-    for (int i = i0; i < i1; ++i) {
-        ngt += keys[i] > T;
-        neq += keys[i] == T;
-    }
-    int cta_gt, cta_eq;
-    block_exclusive_scan(ngt, sh.scan, cta_gt);
-    const int eq_pre = block_exclusive_scan(neq, sh.scan, cta_eq);
-    if (tid == 0) {
-        sh.cnt[0] = cta_gt;
-        sh.cnt[1] = cta_eq;
-    }
-    cluster_sync_all();
-    int base_gt = 0, base_eq = 0;
-    {
-        uint32_t cg[CL], ce[CL];
-#pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) {
-            cg[r] = r < rank ? ld_dsmem_u32(dsmem_addr(&sh.cnt[0], r)) : 0u;
-            ce[r] = r < rank ? ld_dsmem_u32(dsmem_addr(&sh.cnt[1], r)) : 0u;
-        }
-#pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) {
-            base_gt += static_cast<int>(cg[r]);
-            base_eq += static_cast<int>(ce[r]);
-        }
-    }
-    const int take_cta = max(0, min(remaining - base_eq, cta_eq));
-    const int pos0 = base_gt + min(base_eq, remaining);
-    const int take_thr = max(0, min(take_cta - eq_pre, neq));
-    int dummy;
-    const int sel_pre = block_exclusive_scan(ngt + take_thr, sh.scan, dummy);
-    int pos = pos0 + sel_pre, eq_seen = eq_pre;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t key = keys[i];
-        const bool keep = key > T || (key == T && eq_seen < take_cta);
-        eq_seen += key == T;
-        if (keep) {
-            if (pos < K) out[pos] = j0 + i;   // pos < K always; the guard only bounds a logic error
-            ++pos;
-        }
-    }
-    cluster_sync_all();   // keep this CTA's counters alive for the others
+    // T = prefix is the K-th largest key; the first `remaining` keys equal to it are
+    // kept. This CTA keeps its keys > T and its first take_cta keys == T, written from
+    // position pos0 on (the kept keys of lower-ranked CTAs come first).
+    const int take_cta = max(0, min(remaining - eq_low, eq_own));
+    const int pos0 = gt_low + min(eq_low, remaining);
+    ordered_keep(keys, nloc, prefix, take_cta, sh, [&](int i, int pos) {
+        if (pos0 + pos < K) out[pos0 + pos] = j0 + i;   // always < K; the guard only bounds a logic error
+    });
     return K;
 }
-
 // ------------------------------------------------------------- attention
 template <int CL, int GM>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
@@ -567,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(SelectAttend
 
     if constexpr (MODE == SAMode::kSelect) {
         select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
+        cluster_sync_all();   // this CTA's shared data stays readable until every CTA is done with it
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
         attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, false,
