@@ -172,7 +172,12 @@ def recorded_traffic(kernel: str):
         return None
     from sparse_kv_page_gb300 import build as B
     ent = rec.get(kernel)
-    if not ent or ent.get("source_fingerprint") != B._fingerprint()[:16]:
+    if not ent:
+        return None
+    try:
+        if ent.get("source_hash") != B.source_hash(ent.get("sources", []))[:16]:
+            return None   # the kernel changed since the counters were taken
+    except OSError:
         return None
     return ent
 

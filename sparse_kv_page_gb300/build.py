@@ -52,6 +52,19 @@ def _fingerprint() -> str:
     return h.hexdigest()
 
 
+def source_hash(names) -> str:
+    """SHA-256 (hex) of the named files under csrc/ or include/, in the order given:
+    identifies a kernel's source independently of the machine that builds it."""
+    h = hashlib.sha256()
+    for n in names:
+        path = os.path.join(CSRC, n)
+        if not os.path.exists(path):
+            path = os.path.join(INCLUDE, n)
+        with open(path, "rb") as fh:
+            h.update(n.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile (if sources changed) and return the library path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
