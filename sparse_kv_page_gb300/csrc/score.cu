@@ -273,12 +273,10 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                     }
                 }
                 const float smu_row = __shfl_sync(0xffffffffu, s_mu, gid);
-                float score_out[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) score_out[nt] = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // MMA1 rows 0-7: ranks of unit i, rows 8-15: ranks of unit i + 4
+                // Per-token logits (log2 domain) of units i and i + 4: MMA1 gives V^T q for both
+                // (rows 0-7 and 8-15), MMA2 reconstructs the 16 tokens of each; `use(u, nt, x0, x1)`
+                // gets this lane's two tokens (gid, gid + 8) of unit u for head 4 nt + t.
+                auto pair_logits = [&](int i, auto&& use) {
                     const uint4 va = *reinterpret_cast<const uint4*>(stg + kStBasis + (ubase + i * HKV) * 512 + lane * 16);
                     const uint4 vb =
                         *reinterpret_cast<const uint4*>(stg + kStBasis + (ubase + (i + 4) * HKV) * 512 + lane * 16);
@@ -318,34 +316,67 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                             float d2[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_f16_1688(d2, ca0, ca1, bw);
                             const float f = fc * qsc[nt];
-                            const float x0 = (d2[0] + d2[1]) * f;
-                            const float x1 = (d2[2] + d2[3]) * f;
-                            // log2-sum-exp2 over the 16 tokens (8 lanes x 2); the sum is taken
-                            // unshifted and redone with the max factored out only if it leaves
-                            // [2^-100, 2^100] (exact either way up to exp2/log2 rounding)
-                            float z = fast_exp2(x0) + fast_exp2(x1);
+                            use(u, nt, (d2[0] + d2[1]) * f, (d2[2] + d2[3]) * f);
+                        }
+                    }
+                };
+                // log2-sum-exp2 over each unit's 16 tokens (8 lanes x 2), taken unshifted: every
+                // lane keeps its partial sum for all 8 units, and a reduce-scatter over the 8 lanes
+                // of its column (lane bits 2-4 = gid) leaves unit gid's total in lane gid.
+                // The first level (lane bit 4) is taken as soon as units i and i + 4 are done.
+                const bool b2 = (gid & 4) != 0, b1 = (gid & 2) != 0, b0 = (gid & 1) != 0;
+                float y4[NT][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float zlo[NT], zhi[NT];   // this lane's partial sums of units i and i + 4
+                    pair_logits(i, [&](int u, int nt, float x0, float x1) {
+                        const float z = fast_exp2(x0) + fast_exp2(x1);
+                        if (u == i)
+                            zlo[nt] = z;
+                        else
+                            zhi[nt] = z;
+                    });
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        y4[nt][i] = (b2 ? zhi[nt] : zlo[nt]) + __shfl_xor_sync(0xffffffffu, b2 ? zlo[nt] : zhi[nt], 16);
+                }
+                float lse[NT];
+                bool out_of_range = false;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float y2[2];
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const float send = b1 ? y4[nt][q2] : y4[nt][q2 + 2];
+                        y2[q2] = (b1 ? y4[nt][q2 + 2] : y4[nt][q2]) + __shfl_xor_sync(0xffffffffu, send, 8);
+                    }
+                    const float z = (b0 ? y2[1] : y2[0]) + __shfl_xor_sync(0xffffffffu, b0 ? y2[0] : y2[1], 4);
+                    out_of_range |= !(z >= 7.9e-31f && z <= 1.26e30f);
+                    lse[nt] = fast_log2(z) * kLn2;
+                }
+                if (__any_sync(0xffffffffu, out_of_range)) {
+                    // some unit's sum left [2^-100, 2^100]: redo every unit with its max factored
+                    // out (exact either way up to exp2/log2 rounding)
+#pragma unroll 1
+                    for (int i = 0; i < 4; ++i)
+                        pair_logits(i, [&](int u, int nt, float x0, float x1) {
+                            float m = fmaxf(x0, x1);
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            float z = fast_exp2(x0 - m) + fast_exp2(x1 - m);
                             z += __shfl_xor_sync(0xffffffffu, z, 4);
                             z += __shfl_xor_sync(0xffffffffu, z, 8);
                             z += __shfl_xor_sync(0xffffffffu, z, 16);
-                            float m = 0.f;
-                            if (__any_sync(0xffffffffu, !(z >= 7.9e-31f && z <= 1.26e30f))) {
-                                m = fmaxf(x0, x1);
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                                z = fast_exp2(x0 - m) + fast_exp2(x1 - m);
-                                z += __shfl_xor_sync(0xffffffffu, z, 4);
-                                z += __shfl_xor_sync(0xffffffffu, z, 8);
-                                z += __shfl_xor_sync(0xffffffffu, z, 16);
-                            }
-                            const float lse_dev = (m + fast_log2(z)) * kLn2;
-                            if (gid == u) {
-                                const float a_raw = fmaf(accmu[nt][0] + accmu[nt][1], 16777216.f, -128.f * qsum[nt]);
-                                const float a_term = a_raw * smu_row * qsc[nt] * kInvSqrtD;
-                                score_out[nt] = a_term + lse_dev;
-                            }
-                        }
-                    }
+                            if (gid == u) lse[nt] = (m + fast_log2(z)) * kLn2;
+                        });
+                }
+                // score of unit gid, head 4 nt + t: centroid term + token LSE
+                float score_out[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float a_raw = fmaf(accmu[nt][0] + accmu[nt][1], 16777216.f, -128.f * qsum[nt]);
+                    score_out[nt] = a_raw * smu_row * qsc[nt] * kInvSqrtD + lse[nt];
                 }
                 if (a.lse_partials) {
                     // (max, sum exp) of this warp's 8 pages for each head: one partial per 8-page block
