@@ -232,10 +232,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 // Split x into a high and a low f16 part: x ~= hi + lo to ~22 significant bits.
+// x as an f16 high part (low 16 bits) and low part (high 16 bits), together
+// about 21 significant bits: the high part is x with its 13 lowest mantissa bits
+// cleared (exact in f16 for 2^-14 <= |x| < 65520), the low part the rounded
+// remainder; both converted by one cvt.rn.f16x2.f32.
 __device__ __forceinline__ uint32_t split_f16_hilo(float x) {
-    __half h = __float2half_rn(x);
-    __half l = __float2half_rn(x - __half2float(h));
-    return pack_f16x2(h, l);
+    const float hi = __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+    const float lo = x - hi;
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(lo), "f"(hi));
+    return d;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

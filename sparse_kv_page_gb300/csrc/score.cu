@@ -244,13 +244,15 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
             const int nv = min(8, nvalid - 8 * blk);
             if (nv > 0) {
                 const int ubase = (8 * blk) * HKV + kvh;   // stage unit index of the warp's unit 0
-                // scales of unit `lane` (lanes 0..7); zero for units past the end
-                float s_mu = 0.f, s_v = 0.f, s_c = 0.f;
+                // scales of unit `lane` (lanes 0..7); zero for units past the end. The token
+                // logits of a unit carry s_V s_C / sqrt(d) (log2 domain): one factor per unit.
+                float s_mu = 0.f, s_vc = 0.f;
                 if (lane < nv) {
                     const uint2 sc = *reinterpret_cast<const uint2*>(stg + kStScales + (ubase + lane * HKV) * 8);
                     s_mu = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x & 0xffffu)));
-                    s_v = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x >> 16)));
-                    s_c = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.y & 0xffffu)));
+                    s_vc = __half2float(__ushort_as_half(static_cast<unsigned short>(sc.x >> 16))) *
+                           __half2float(__ushort_as_half(static_cast<unsigned short>(sc.y & 0xffffu))) *
+                           (kInvSqrtD * kLog2e);
                 }
                 // centroid term: rows = the warp's 8 units, K = 128 dims
                 float accmu[NT][4];
@@ -301,21 +303,20 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int u = i + 4 * half;
-                        const float svu = __shfl_sync(0xffffffffu, s_v, u);
-                        const float fc = __shfl_sync(0xffffffffu, s_c, u) * (kInvSqrtD * kLog2e);
+                        const float fvc = __shfl_sync(0xffffffffu, s_vc, u);
                         const uint32_t cw =
                             *reinterpret_cast<const uint32_t*>(stg + kStCoef + (ubase + u * HKV) * 128 + lane * 4);
                         uint32_t ca0, ca1;
                         int8x4_to_f16x2(cw, ca0, ca1);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            // W' = s_V (sum_k (x_k + 8) q'_k - 8 sum_k q'_k); the MMA sum carries 2^-24
+                            // W = sum_k (x_k + 8) q'_k - 8 sum_k q'_k (|W| < 3000); the MMA sum carries 2^-24
                             const float raw = half == 0 ? acc[nt][0] + acc[nt][1] : acc[nt][2] + acc[nt][3];
-                            const float w = fmaf(raw, 16777216.f, -8.f * qsum[nt]) * svu;
+                            const float w = fmaf(raw, 16777216.f, -8.f * qsum[nt]);
                             const uint32_t bw = movmatrix_trans(split_f16_hilo(w));
                             float d2[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_f16_1688(d2, ca0, ca1, bw);
-                            const float f = fc * qsc[nt];
+                            const float f = fvc * qsc[nt];
                             use(u, nt, (d2[0] + d2[1]) * f, (d2[2] + d2[3]) * f);
                         }
                     }
