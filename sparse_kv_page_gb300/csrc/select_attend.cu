@@ -36,6 +36,7 @@ constexpr int kRingBytes = kWarps * kPageSlotBytes;   // 69,632 B
 constexpr int kPartStride = 2 + kD;                   // m, l, o[128]
 constexpr int kMaxG = LOCKS_MAX_GROUP;
 constexpr int kQRow = 136;                            // bf16 per staged query row (128 + 8 pad)
+constexpr int kRankCap = 256;                         // radix early exit: largest bin ranked directly
 
 struct SmallShared {
     uint16_t qs[2][16 * kQRow];           // query rows (group heads), bf16 high / low parts
@@ -45,7 +46,12 @@ struct SmallShared {
     float red_m[kWarps][kMaxG], red_l[kWarps][kMaxG];
     uint32_t tot[3][256];                 // radix pass: bin counts of all CTAs, lower-ranked CTAs, this CTA
     int wcnt[kWarps][2];
-    int digit, above, above_low, above_own, eq_low, eq_own;
+    int digit, above, above_low, above_own, eq_low, eq_own, inbin;
+    // radix early exit: the chosen bin's keys (this CTA's, then all CTAs')
+    int bin_cnt[16], nbin, rank_take, cnt4[4];
+    uint32_t rank_T;
+    uint32_t bin_keys[256], rank_keys[256];
+    uint8_t rank_src[256];
     uint64_t bar[kWarps];
     float cpart[kMaxG * kPartStride];     // this CTA's attention partial per head
 };
@@ -64,9 +70,33 @@ __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float 
 // one batch ahead (the first one before the normaliser's reduction, so its
 // latency overlaps the cluster exchange). Loops stay rolled: this code runs
 // about once per launch, and its instruction fetch is what it waits on.
+// Stores the group's query rows (scaled by log2(e)/sqrt(d)) in shared memory as bf16
+// high and low parts; the attention's MMA A fragments are read back with ldmatrix.
+__device__ __forceinline__ void store_query(const float (&qv)[16 * kD / kThreads], int g, SmallShared& sh) {
+#pragma unroll
+    for (int u = 0; u < 16 * kD / kThreads; ++u) {
+        const int idx = threadIdx.x + u * kThreads, row = idx / kD, col = idx % kD;
+        const float x = row < g ? qv[u] * (kInvSqrtD * kLog2e) : 0.f;
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(h));
+        sh.qs[0][row * kQRow + col] = __bfloat16_as_ushort(h);
+        sh.qs[1][row * kQRow + col] = __bfloat16_as_ushort(lo);
+    }
+}
+__device__ __forceinline__ void load_query(const SelectAttendArgs& a, int b, int kvh, int g,
+                                           float (&qv)[16 * kD / kThreads]) {
+#pragma unroll
+    for (int u = 0; u < 16 * kD / kThreads; ++u) {
+        const int idx = threadIdx.x + u * kThreads, row = idx / kD, col = idx % kD;
+        qv[u] = row < g ? a.q[(static_cast<int64_t>(b) * a.hq + kvh * g + row) * kD + col] : 0.f;
+    }
+}
+
+// stage_q: also stage the query rows for the attention that follows (their loads
+// overlap the normaliser's).
 template <int CL, int GM>
 __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, uint32_t* keys,
-                           SmallShared& sh) {
+                           SmallShared& sh, bool stage_q) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = a.hq / a.hkv;
     const int nloc = j1 - j0;
@@ -84,6 +114,8 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
     };
     float v[kB][GM];
     load_batch(v, j0 + tid);
+    float qv[16 * kD / kThreads];
+    if (stage_q) load_query(a, b, kvh, g, qv);
 
     // 1. per-head log-sum-exp over the sequence's pages: (m, l) per thread and head
     float m[GM], l[GM];
@@ -137,6 +169,7 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
             }
         }
     }
+    if (stage_q) store_query(qv, g, sh);   // read after the barriers below
     // warp reduction: max first, then the sums rescaled to it
 #pragma unroll
     for (int hh = 0; hh < GM; ++hh) {
@@ -310,14 +343,14 @@ __device__ int ordered_keep(const uint32_t* keys, int n, uint32_t T, int take_eq
 // without a further exchange.
 template <int CL, int GM>
 __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk, uint32_t* keys,
-                            SmallShared& sh) {
+                            SmallShared& sh, bool stage_q) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = max(0, min(a.seq_pages[b], a.max_pages));
     const int j0 = min(P, static_cast<int>(rank) * chunk);
     const int j1 = min(P, j0 + chunk);
     const int nloc = j1 - j0;
 
-    group_keys<CL, GM>(a, b, kvh, j0, j1, keys, sh);
+    group_keys<CL, GM>(a, b, kvh, j0, j1, keys, sh, stage_q);
 
     int K = min(a.budget_pages, min(P, a.k_cap));
     K = max(K, 0);
@@ -403,6 +436,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
                     sh.above_own = ab[2];
                     sh.eq_low = c[1][i];
                     sh.eq_own = c[2][i];
+                    sh.inbin = c[0][i];
                 }
 #pragma unroll
                 for (int k = 0; k < 3; ++k) ab[k] += c[k][i];
@@ -415,6 +449,73 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
         gt_own += sh.above_own;
         eq_low = sh.eq_low;
         eq_own = sh.eq_own;
+        const int inbin = sh.inbin;
+        if (pass < 3 && inbin <= kRankCap) {
+            // The K-th largest key is one of the inbin keys of the chosen bin: every CTA
+            // publishes its keys of that bin, every CTA gathers all of them through DSMEM and
+            // ranks them directly instead of running the remaining passes.
+            if (tid == sh.digit) {
+#pragma unroll
+                for (uint32_t r = 0; r < CL; ++r) sh.bin_cnt[r] = static_cast<int>(hv[r]);
+            }
+            if (tid == 0) sh.nbin = 0;
+            __syncthreads();
+            const uint32_t want = prefix >> shift;   // every bit at or above this pass's digit
+            for (int i0 = 0; i0 < nloc; i0 += kThreads) {
+                const int i = i0 + tid;
+                const uint32_t key = i < nloc ? keys[i] : 0u;
+                const bool m = i < nloc && (key >> shift) == want;
+                const unsigned bal = __ballot_sync(0xffffffffu, m);
+                int base = 0;
+                if (lane == 0 && bal) base = atomicAdd(&sh.nbin, __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (m) sh.bin_keys[base + __popc(bal & lanemask_lt())] = key;
+            }
+            cluster_sync_all();   // every CTA's bin keys are complete and visible
+            if (tid < inbin) {
+                int r = 0, base = 0;
+#pragma unroll
+                for (int q = 0; q < CL - 1; ++q) {
+                    if (r == q && tid >= base + sh.bin_cnt[q]) {   // past rank q's keys: move on
+                        base += sh.bin_cnt[q];
+                        r = q + 1;
+                    }
+                }
+                sh.rank_keys[tid] = ld_dsmem_u32(dsmem_addr(&sh.bin_keys[tid - base], static_cast<uint32_t>(r)));
+                sh.rank_src[tid] = static_cast<uint8_t>(r);
+            }
+            if (tid < 4) sh.cnt4[tid] = 0;
+            __syncthreads();
+            if (tid < inbin) {
+                const uint32_t key = sh.rank_keys[tid];
+                int gt = 0, ge = 0;
+                for (int q = 0; q < inbin; ++q) {
+                    const uint32_t v = sh.rank_keys[q];
+                    gt += v > key;
+                    ge += v >= key;
+                }
+                if (gt < remaining && ge >= remaining) {   // key is the remaining-th largest of the bin
+                    sh.rank_T = key;
+                    sh.rank_take = remaining - gt;
+                }
+            }
+            __syncthreads();
+            const uint32_t T = sh.rank_T;
+            if (tid < inbin) {
+                const uint32_t key = sh.rank_keys[tid];
+                const int r = sh.rank_src[tid];
+                if ((key >= T) && r <= static_cast<int>(rank))
+                    atomicAdd(&sh.cnt4[(key > T ? 0 : 2) + (r == static_cast<int>(rank) ? 1 : 0)], 1);
+            }
+            __syncthreads();
+            gt_low += sh.cnt4[0];
+            gt_own += sh.cnt4[1];
+            eq_low = sh.cnt4[2];
+            eq_own = sh.cnt4[3];
+            prefix = T;
+            remaining = sh.rank_take;
+            break;
+        }
     }
     // T = prefix is the K-th largest key; the first `remaining` keys equal to it are
     // kept. This CTA keeps its keys > T and its first take_cta keys == T, written from
@@ -429,7 +530,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
 // ------------------------------------------------------------- attention
 template <int CL, int GM>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
-                             const int32_t* sel, bool sel_coherent, uint8_t* ring, SmallShared& sh) {
+                             const int32_t* sel, bool sel_coherent, bool q_staged, uint8_t* ring, SmallShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, t = lane & 3;
     const int g = a.hq / a.hkv;
@@ -437,18 +538,10 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     const int p0 = min(n_sel, static_cast<int>(rank) * per);
     const int p1 = min(n_sel, p0 + per);
 
-    // query rows of the group (scaled by log2(e)/sqrt(d)) staged in shared memory as bf16
-    // high and low parts; the MMA A fragments are read back with ldmatrix
-    {
-        const float c = kInvSqrtD * kLog2e;
-        for (int idx = tid; idx < 16 * kD; idx += kThreads) {
-            const int row = idx / kD, col = idx % kD;
-            const float x = row < g ? a.q[(static_cast<int64_t>(b) * a.hq + kvh * g + row) * kD + col] * c : 0.f;
-            const __nv_bfloat16 h = __float2bfloat16_rn(x);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(h));
-            sh.qs[0][row * kQRow + col] = __bfloat16_as_ushort(h);
-            sh.qs[1][row * kQRow + col] = __bfloat16_as_ushort(lo);
-        }
+    if (!q_staged) {
+        float qv[16 * kD / kThreads];
+        load_query(a, b, kvh, g, qv);
+        store_query(qv, g, sh);
         __syncthreads();
     }
     const int qrow = (lane & 7) + ((lane >> 3) & 1) * 8, qcol = (lane >> 4) * 8;
@@ -651,19 +744,19 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(SelectAttend
     __syncthreads();
 
     if constexpr (MODE == SAMode::kSelect) {
-        select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
+        select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh, false);
         cluster_sync_all();   // this CTA's shared data stays readable until every CTA is done with it
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
         attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, false,
-                         big, sh);
+                             false, big, sh);
     } else {
-        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh);
+        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh, true);
         // the selection went to global memory; make it visible to the cluster's CTAs
         asm volatile("fence.acq_rel.cluster;" ::: "memory");
         cluster_sync_all();
         attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, true,
-                         big, sh);
+                             true, big, sh);
     }
 }
 
