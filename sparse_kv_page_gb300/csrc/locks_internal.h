@@ -1,6 +1,7 @@
 // locks_internal.h - launchers shared between the kernel files and the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -67,6 +68,9 @@ struct SelectAttendArgs {
     float* lse;               // nullable
     int batch, hq, hkv, max_pages, num_phys;
     DeviceStatus st;
+    // K and V caches as 2D tensors [num_phys * hkv * 16 rows][128] bf16 for tiled TMA:
+    // 64 x 16 boxes with 128-byte swizzle (filled by the launcher; unused by the selection)
+    CUtensorMap tm_k, tm_v;
 };
 enum class SAMode { kSelect, kAttend, kSelectAttend };
 cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream);

@@ -23,6 +23,10 @@
 // When the scoring kernel's per-8-page LSE partials are given, the per-head
 // normaliser L_h is reduced from them instead of from the full score table.
 // At most 128 registers per thread so that two CTAs share an SM.
+#include <cudaTypedefs.h>
+#include <climits>
+#include <cstring>
+
 #include "locks_internal.h"
 
 namespace locks {
@@ -30,10 +34,16 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowBytes = 272;                        // 256 B row + 16 B pad (conflict-free ldmatrix)
-constexpr int kPageSlotBytes = 2 * kPage * kRowBytes; // K rows then V rows: 8704 B
-constexpr int kRingBytes = kWarps * kPageSlotBytes;   // 69,632 B
+// A page slot holds the page's K then V rows of one kv head as four TMA boxes of
+// 16 rows x 64 dims (128-byte rows, 128-byte swizzle: 16-byte chunk c of row r
+// sits at chunk c ^ (r & 7)), each 2 KiB and 1 KiB-aligned.
+constexpr int kBoxBytes = kPage * 64 * 2;             // 2048 B
+constexpr int kPageSlotBytes = 4 * kBoxBytes;         // 8192 B
 constexpr int kPartStride = 2 + kD;                   // m, l, o[128]
+// the ring also holds the warps' attention partials after the page loop
+constexpr int kWarpPartBytes = kWarps * LOCKS_MAX_GROUP * kPartStride * 4;
+constexpr int kRingBytes = ((kWarps * kPageSlotBytes > kWarpPartBytes ? kWarps * kPageSlotBytes : kWarpPartBytes) +
+                            1023) / 1024 * 1024;
 constexpr int kMaxG = LOCKS_MAX_GROUP;
 constexpr int kQRow = 136;                            // bf16 per staged query row (128 + 8 pad)
 constexpr int kRankCap = 256;                         // radix early exit: largest bin ranked directly
@@ -55,6 +65,12 @@ struct SmallShared {
     uint64_t bar[kWarps];
     float cpart[kMaxG * kPartStride];     // this CTA's attention partial per head
 };
+
+// Byte offset of (token row, dim) in a page slot's K (or V) half: box = dim / 64,
+// 16-byte chunk (dim % 64) / 8 swizzled with the row.
+__device__ __forceinline__ int swz_offset(int token, int dim) {
+    return (dim >> 6) * kBoxBytes + token * 128 + ((((dim & 63) >> 3) ^ (token & 7)) << 4);
+}
 
 __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
     const float M = fmaxf(m, m2);
@@ -554,7 +570,6 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     uint64_t* bar = &sh.bar[warp];
     uint32_t phase = 0;
     bool failed = false, bad = false;
-    const int64_t head_stride = static_cast<int64_t>(kPage) * kD;   // elements per (page, kv head)
     for (int p = p0 + warp; p < p1; p += kWarps) {
         int logical = sel_coherent ? __ldcg(sel + p) : sel[p];
         if (logical < 0 || logical >= a.max_pages) {
@@ -566,19 +581,20 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             bad = true;
             phys = 0;
         }
-        const int64_t off = (phys * a.hkv + kvh) * head_stride;
+        const int y = static_cast<int>((phys * a.hkv + kvh) * kPage);   // first row of the page's tile
         fence_proxy_async_smem();   // earlier generic reads of the slot before the async refill
-        if (lane == 0) mbar_arrive_expect_tx(bar, 2 * kPage * kD * 2);
         __syncwarp();
-        {
-            const int row = lane & 15;
-            const uint16_t* src = (lane < 16 ? a.k_cache : a.v_cache) + off + row * kD;
-            bulk_g2s(slot + (lane < 16 ? 0 : kPage * kRowBytes) + row * kRowBytes, src, kD * 2, bar);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, kPageSlotBytes);
+            tma_load_2d(slot, &a.tm_k, 0, y, bar);
+            tma_load_2d(slot + kBoxBytes, &a.tm_k, 64, y, bar);
+            tma_load_2d(slot + 2 * kBoxBytes, &a.tm_v, 0, y, bar);
+            tma_load_2d(slot + 3 * kBoxBytes, &a.tm_v, 64, y, bar);
         }
         if (!mbar_wait_bounded(bar, phase, a.st.wait_limit_ns)) failed = true;
         phase ^= 1u;
         const uint8_t* kslot = slot;
-        const uint8_t* vslot = slot + kPage * kRowBytes;
+        const uint8_t* vslot = slot + 2 * kBoxBytes;
 
         // S = Q K^T: two n-tiles of 8 tokens
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -588,7 +604,7 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             const int mat = lane >> 3;
             const int token = (mat >> 1) * 8 + (lane & 7);
             const int dim = 16 * s + (mat & 1) * 8;
-            ldmatrix_x4(kb, kslot + token * kRowBytes + dim * 2);
+            ldmatrix_x4(kb, kslot + swz_offset(token, dim));
             ldmatrix_x4(qh, &sh.qs[0][qrow * kQRow + 16 * s + qcol]);
             ldmatrix_x4(ql, &sh.qs[1][qrow * kQRow + 16 * s + qcol]);
             mma_bf16_16816(sacc[0], qh, kb[0], kb[1]);
@@ -634,7 +650,7 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             const int mat = lane >> 3;
             const int token = (mat & 1) * 8 + (lane & 7);
             const int dim = 8 * (nd + (mat >> 1));
-            ldmatrix_x4_trans(vb, vslot + token * kRowBytes + dim * 2);
+            ldmatrix_x4_trans(vb, vslot + swz_offset(token, dim));
             mma_bf16_16816(o[nd], pa, vb[0], vb[1]);
             mma_bf16_16816(o[nd + 1], pa, vb[2], vb[3]);
         }
@@ -732,10 +748,13 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
 }
 
 template <int CL, SAMode MODE, int GM>
-__global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(SelectAttendArgs a, int chunk) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid_constant__ SelectAttendArgs a,
+                                                                       int chunk) {
+    extern __shared__ __align__(1024) uint8_t smem[];
     SmallShared& sh = *reinterpret_cast<SmallShared*>(smem);
-    uint8_t* big = smem + ((sizeof(SmallShared) + 127) / 128) * 128;
+    // the region after SmallShared, 1 KiB-aligned in the shared window (128-byte swizzle)
+    const uint32_t small_end = smem_u32(smem) + static_cast<uint32_t>(sizeof(SmallShared));
+    uint8_t* big = smem + (((small_end + 1023u) & ~1023u) - smem_u32(smem));
     const uint32_t rank = cluster_ctarank();
     const int seg = blockIdx.y;
     const int b = seg / a.hkv, kvh = seg % a.hkv;
@@ -765,8 +784,49 @@ int chunk_of(int max_pages, int cluster) {
     return (c + 7) & ~7;   // whole 8-page blocks (the LSE partials' granularity)
 }
 
+// The driver's tiled tensor-map encoder, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// A K or V cache [num_phys][hkv][16][128] bf16 as a 2D tensor of num_phys * hkv * 16
+// rows of 128 elements, read in 64 x 16 boxes with 128-byte swizzle.
+cudaError_t encode_cache_map(CUtensorMap* map, const uint16_t* base, int64_t rows) {
+    const auto fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box,
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int CL, SAMode MODE, int GM>
-cudaError_t launch_t(const SelectAttendArgs& a, cudaStream_t stream) {
+cudaError_t launch_t(const SelectAttendArgs& args, cudaStream_t stream) {
+    SelectAttendArgs a = args;
+    std::memset(&a.tm_k, 0, sizeof(a.tm_k));
+    std::memset(&a.tm_v, 0, sizeof(a.tm_v));
+    if (MODE != SAMode::kSelect) {
+        const int64_t rows = static_cast<int64_t>(a.num_phys) * a.hkv * kPage;   // TMA row coordinates are int32
+        if (rows > INT_MAX) return cudaErrorInvalidValue;
+        cudaError_t e = encode_cache_map(&a.tm_k, a.k_cache, rows);
+        if (e == cudaSuccess) e = encode_cache_map(&a.tm_v, a.v_cache, rows);
+        if (e != cudaSuccess) return e;
+    }
     const int chunk = chunk_of(a.max_pages, CL);
     const size_t smem = select_attend_smem_bytes(a.max_pages, CL, MODE);
     auto kern = select_attend_kernel<CL, MODE, GM>;
@@ -834,7 +894,7 @@ int active_clusters_cl(size_t smem, SAMode mode) {
 }  // namespace
 
 size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode) {
-    const size_t small = ((sizeof(SmallShared) + 127) / 128) * 128;
+    const size_t small = sizeof(SmallShared) + 1024;   // + alignment of the region after it
     const size_t keys = (mode == SAMode::kAttend) ? 0 : static_cast<size_t>(chunk_of(max_pages, cluster)) * 4;
     const size_t ring = (mode == SAMode::kSelect) ? 0 : static_cast<size_t>(kRingBytes);
     return small + (keys > ring ? keys : ring);
