@@ -423,10 +423,48 @@ def run_locks(args, rank, world, local):
             e2e_us.append((time.perf_counter() - t1) * 1e6)
     e2e_value = reduce_max(statistics.mean(e2e_us), world, dev)
 
+    # dense comparator (outside the timed region): the same attention kernel with every page
+    # of every sequence selected, i.e. exact attention over the whole cache
+    dense = None
+    if not args.no_dense:
+        k_cap_all = L.locks_k_cap(dims, w.pages * 16)
+        sel_all = torch.arange(w.pages, dtype=torch.int32, device=dev).repeat(w.batch * w.num_kv_heads, 1)
+        sel_all = sel_all.view(w.batch, w.num_kv_heads, w.pages)[:, :, :k_cap_all].contiguous()
+        nsel_all = seq.view(-1, 1).repeat(1, w.num_kv_heads).to(torch.int32).contiguous()
+        out_d = torch.empty_like(out)
+
+        def dense_attention():
+            L.locks_sparse_attention(dims, q, kc, vc, table, sel_all, nsel_all, k_cap_all, out_d, None, ws)
+
+        dense_attention()
+        g_dense = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_dense):
+            dense_attention()
+        n_dense = max(3, min(K, 20))
+        d_us = []
+        for i in range(n_dense + 2):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            g_dense.replay()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                d_us.append(a_.elapsed_time(b_) * 1000.0)
+        dense_us = reduce_max(statistics.mean(d_us), world, dev)
+        dense_bytes = int(inp.seq_pages.astype(np.int64).sum()) * w.num_kv_heads * PAGE_KV_BYTES
+        dense = {"attention_us": dense_us, "kv_bytes": dense_bytes, "GBps": dense_bytes / (dense_us * 1e-6) / 1e9,
+                 "steps": n_dense, "locks_step_speedup": dense_us / mean_step_us,
+                 "path": "locks_sparse_attention with every page selected (exact attention over the whole cache, "
+                         "same attention kernel), one CUDA graph, L2 flushed before each"}
+        assert L.locks_get_device_status(ws) == 0, "device status after the dense comparator"
+
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    if dense:
+        dense["frac_of_measured_hbm"] = dense["GBps"] / hbm
     summ_bytes, kv_bytes = algorithmic_bytes(w, budget)
     step_bytes = summ_bytes + kv_bytes
     score_gbs = summ_bytes / (mean_score_us * 1e-6) / 1e9
@@ -447,6 +485,7 @@ def run_locks(args, rank, world, local):
         "kernels_us": {"score_pages": mean_score_us, "select_attend": mean_sa_us,
                        "step_p50": statistics.median(step_ms) * 1000.0},
         "bytes_vs_dense": (w.batch * w.pages * w.num_kv_heads * PAGE_KV_BYTES) / step_bytes,
+        "dense_comparator": dense,
         "roofline": {"kernel": "score_pages (locks_score_pages)", "bound": "hbm", "achieved": score_gbs,
                      "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": score_gbs / hbm,
@@ -476,6 +515,7 @@ def main(argv=None):
     ap.add_argument("--budget", type=int, default=None)
     ap.add_argument("--pages", type=int, default=None, help="override pages per sequence (smaller cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -205,6 +205,45 @@ def test_attention_parity(g, hkv, n_list):
                 assert abs(lse_g[b, h] - ref_lse[b, h]) < 1e-3
 
 
+def test_attention_all_pages_is_dense_attention():
+    """Every page selected (the dense comparator's path, many pages per warp): the output
+    is textbook softmax attention over all of each sequence's tokens."""
+    rng = np.random.default_rng(41)
+    B, hkv, g, maxp = 2, 2, 4, 1500
+    seq = np.array([1500, 913], np.int32)
+    nphys = B * maxp
+    kc = synth.f32_to_bf16_bits(rng.standard_normal((nphys, hkv, 16, 128)).astype(np.float32))
+    vc = synth.f32_to_bf16_bits(rng.standard_normal((nphys, hkv, 16, 128)).astype(np.float32))
+    q = (rng.standard_normal((B, hkv * g, 128)) * 1.5).astype(np.float32)
+    table = rng.permutation(nphys).reshape(B, maxp).astype(np.int32)
+    sel = np.tile(np.arange(maxp, dtype=np.int32), (B, hkv, 1))
+    nsel = np.repeat(seq[:, None], hkv, axis=1).astype(np.int32)
+    prob = device_problem(q, kc, vc, table, seq)
+    out = torch.zeros((B, hkv * g, 128), dtype=torch.int16, device=DEV)
+    lse = torch.zeros((B, hkv * g), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    L.locks_sparse_attention(prob.dims, prob.q, prob.k_cache, prob.v_cache, prob.page_table, t(sel), t(nsel), maxp,
+                             out, lse, ws)
+    torch.cuda.synchronize()
+    assert L.locks_get_device_status(ws) == 0
+    got = bf16_out(out)
+    kf = synth.bf16_bits_to_f32(kc).astype(np.float64)
+    vf = synth.bf16_bits_to_f32(vc).astype(np.float64)
+    lse_g = lse.cpu().numpy()
+    for b in range(B):
+        phys = table[b, :seq[b]]
+        for h in range(hkv * g):
+            keys = kf[phys, h // g].reshape(-1, 128)
+            vals = vf[phys, h // g].reshape(-1, 128)
+            logits = keys @ q[b, h].astype(np.float64) / np.sqrt(128.0)
+            m = logits.max()
+            p = np.exp(logits - m)
+            ref = (p @ vals) / p.sum()
+            assert np.abs(got[b, h] - ref).max() < ATT_ABS
+            assert cosine(got[b, h], ref) >= ATT_COS
+            assert abs(lse_g[b, h] - (m + np.log(p.sum()))) < 1e-3
+
+
 # ----------------------------------------------------------- fused step
 
 def _run_decode(w, inp, mu, basis, coef, scales, budget):
