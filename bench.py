@@ -423,6 +423,38 @@ def run_locks(args, rank, world, local):
             e2e_us.append((time.perf_counter() - t1) * 1e6)
     e2e_value = reduce_max(statistics.mean(e2e_us), world, dev)
 
+    # full-model decode graph (outside the timed region): 32 layers' decode steps (score +
+    # select_attend each) in one CUDA graph, each layer streaming the same resident buffers
+    # (far larger than L2, so every layer reads its summaries and K/V from HBM)
+    model_graph = None
+    if not args.no_model_graph:
+        n_layers = 32
+        g_model = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_model):
+            for _ in range(n_layers):
+                score()
+                select_attend()
+        g_model.replay()
+        torch.cuda.synchronize()
+        m_us = []
+        for i in range(5):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            g_model.replay()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            if i >= 1:
+                m_us.append(a_.elapsed_time(b_) * 1000.0)
+        model_us = reduce_max(statistics.mean(m_us), world, dev)
+        model_graph = {"layers": n_layers, "us": model_us, "per_layer_us": model_us / n_layers,
+                       "per_layer_vs_single_step": (model_us / n_layers) / mean_step_us, "replays": len(m_us),
+                       "path": "32 x (score_pages, select_attend) captured in one CUDA graph on the same "
+                               "buffers, L2 flushed before each replay; the summaries stream from HBM in "
+                               "every layer, the selected K/V pages (k x 8 KiB per kv head) of one layer "
+                               "can stay in L2 for the next, which separate layers' caches would not"}
+        assert L.locks_get_device_status(ws) == 0, "device status after the model graph"
+
     # dense comparator (outside the timed region): the same attention kernel with every page
     # of every sequence selected, i.e. exact attention over the whole cache
     dense = None
@@ -486,6 +518,7 @@ def run_locks(args, rank, world, local):
                        "step_p50": statistics.median(step_ms) * 1000.0},
         "bytes_vs_dense": (w.batch * w.pages * w.num_kv_heads * PAGE_KV_BYTES) / step_bytes,
         "dense_comparator": dense,
+        "model_graph": model_graph,
         "roofline": {"kernel": "score_pages (locks_score_pages)", "bound": "hbm", "achieved": score_gbs,
                      "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": score_gbs / hbm,
@@ -516,6 +549,7 @@ def main(argv=None):
     ap.add_argument("--pages", type=int, default=None, help="override pages per sequence (smaller cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
+    ap.add_argument("--no-model-graph", action="store_true", help="skip the 32-layer decode graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
