@@ -77,7 +77,7 @@ def _load() -> ctypes.CDLL:
                 "lo_scores_sampled": ([i32, i32, i32, i32, P, P, P, P, P, P, i64, P, P, P, P], None),
                 "lo_group_keys": ([i32, i32, i32, i32, P, P, P, P], None),
                 "lo_select": ([i32, i32, i32, P, P, i32, i32, P, P], None),
-                "lo_attend": ([i32, i32, i32, i32, P, P, P, P, P, P, i32, P, P], None),
+                "lo_attend": ([i32, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -241,8 +241,9 @@ def select(keys: np.ndarray, seq_pages, budget_tokens: int, k_cap: Optional[int]
 
 # ---------------------------------------------------------------- attention
 
-def attend(q, k_cache, v_cache, page_table, selected, n_selected):
-    """(out [B][Hq][128] float64, lse [B][Hq]) over the selected pages only."""
+def attend(q, k_cache, v_cache, page_table, selected, n_selected, seq_pages=None, tail_tokens=None):
+    """(out [B][Hq][128] float64, lse [B][Hq]) over the selected pages, plus the first
+    tail_tokens[b] tokens of logical page seq_pages[b] (the unfilled page) when given."""
     q = _c(q, np.float32)
     B, Hq, _ = q.shape
     kc, vc = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
@@ -252,16 +253,23 @@ def attend(q, k_cache, v_cache, page_table, selected, n_selected):
     nsel = _c(n_selected, np.int32)
     out = np.zeros((B, Hq, D))
     lse = np.zeros((B, Hq))
+    if tail_tokens is not None:
+        sp, tt = _c(seq_pages, np.int32), _c(tail_tokens, np.int32)
+        psp, ptt = _p(sp), _p(tt)
+    else:
+        psp = ptt = None
     _load().lo_attend(B, Hq, Hkv, table.shape[1], _p(q), _p(kc), _p(vc), _p(table), _p(sel), _p(nsel),
-                      sel.shape[2], _p(out), _p(lse))
+                      sel.shape[2], psp, ptt, _p(out), _p(lse))
     return out, lse
 
 
-def decode_step(q, k_cache, v_cache, page_table, seq_pages, mu, basis, coef, scales, budget_tokens: int):
-    """The whole step in float64: scores -> group keys -> select -> attend."""
+def decode_step(q, k_cache, v_cache, page_table, seq_pages, mu, basis, coef, scales, budget_tokens: int,
+                tail_tokens=None):
+    """The whole step in float64: scores -> group keys -> select -> attend (plus the
+    unfilled page's tail_tokens tokens, attended whole, when given)."""
     Hkv = k_cache.shape[1]
     s = scores(q, mu, basis, coef, scales, page_table, seq_pages, Hkv)
     keys, lse_h = group_keys(s, seq_pages, Hkv)
     sel, nsel = select(keys, seq_pages, budget_tokens)
-    out, lse = attend(q, k_cache, v_cache, page_table, sel, nsel)
+    out, lse = attend(q, k_cache, v_cache, page_table, sel, nsel, seq_pages, tail_tokens)
     return dict(scores=s, keys=keys, head_lse=lse_h, selected=sel, n_selected=nsel, out=out, lse=lse)

@@ -486,17 +486,23 @@ void lo_select(int batch, int hkv, int max_pages, const double* keys, const int3
 /* -------------------------------------------------------------- attention */
 
 /*
- * Attention over the selected pages only [p1 "Code": scaled dot-product
- * attention of q over the gathered keys/values of the chosen pages, default
- * scale 1/sqrt(d)]: for every (b, query head h) with kv head h / g,
- *   l_i = q . k_i / sqrt(128) over the 16 tokens of each selected page,
- *   out = sum_i softmax(l)_i v_i,  lse = log sum_i exp(l_i).
- * An empty selection gives out = 0 and lse = -inf.
- * out is [B][Hq][128], lse [B][Hq] (may be NULL).
+ * Attention over the selected pages [p1 "Code": scaled dot-product attention of
+ * q over the gathered keys/values of the chosen pages, default scale 1/sqrt(d)],
+ * plus, when tail_tokens is given, the first tail_tokens[b] tokens of the
+ * sequence's partially filled page (logical page seq_pages[b]). A page gets its
+ * summary only once it fills [p1 "How LOCKS works": the decomposition runs when
+ * a page fills, every 16 tokens], so the unfilled page cannot be scored; it is
+ * attended whole (the pages are silent on it; this is the plain reading).
+ * For every (b, query head h) with kv head h / g, over that token set:
+ *   l_i = q . k_i / sqrt(128),  out = sum_i softmax(l)_i v_i,  lse = log sum_i exp(l_i).
+ * An empty set gives out = 0 and lse = -inf.
+ * out is [B][Hq][128], lse [B][Hq] (may be NULL); seq_pages and tail_tokens may
+ * both be NULL (no tail).
  */
 void lo_attend(int batch, int hq, int hkv, int max_pages, const float* q, const uint16_t* k_cache,
                const uint16_t* v_cache, const int32_t* page_table, const int32_t* selected,
-               const int32_t* n_selected, int k_cap, double* out, double* lse) {
+               const int32_t* n_selected, int k_cap, const int32_t* seq_pages, const int32_t* tail_tokens,
+               double* out, double* lse) {
     int g = hq / hkv;
     int64_t total = (int64_t)batch * hq;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -504,20 +510,32 @@ void lo_attend(int batch, int hq, int hkv, int max_pages, const float* q, const 
         int b = (int)(bh / hq), h = (int)(bh % hq), kvh = h / g;
         int n = n_selected[b * hkv + kvh];
         const int32_t* sel = selected + ((int64_t)b * hkv + kvh) * k_cap;
+        int tail = (tail_tokens && seq_pages) ? tail_tokens[b] : 0;
         const float* qv = q + bh * LO_D;
         double* o = out + bh * LO_D;
         for (int c = 0; c < LO_D; ++c) o[c] = 0.0;
-        if (n <= 0) {
+        if (n < 0) n = 0;
+        if (n == 0 && tail <= 0) {
             if (lse) lse[bh] = -INFINITY;
             continue;
         }
-        int ntok = n * LO_PAGE;
-        double* logit = (double*)malloc(sizeof(double) * ntok);
-        double mx = -INFINITY;
+        /* the token set: (physical page, tokens used) for each selected page, then the tail */
+        int npages = n + (tail > 0 ? 1 : 0);
+        int64_t* phys = (int64_t*)malloc(sizeof(int64_t) * npages);
+        int* ntok = (int*)malloc(sizeof(int) * npages);
         for (int p = 0; p < n; ++p) {
-            int64_t phys = page_table[(int64_t)b * max_pages + sel[p]];
-            const uint16_t* kp = k_cache + (phys * hkv + kvh) * LO_PAGE * LO_D;
-            for (int i = 0; i < LO_PAGE; ++i) {
+            phys[p] = page_table[(int64_t)b * max_pages + sel[p]];
+            ntok[p] = LO_PAGE;
+        }
+        if (tail > 0) {
+            phys[n] = page_table[(int64_t)b * max_pages + seq_pages[b]];
+            ntok[n] = tail;
+        }
+        double* logit = (double*)malloc(sizeof(double) * npages * LO_PAGE);
+        double mx = -INFINITY;
+        for (int p = 0; p < npages; ++p) {
+            const uint16_t* kp = k_cache + (phys[p] * hkv + kvh) * LO_PAGE * LO_D;
+            for (int i = 0; i < ntok[p]; ++i) {
                 double s = 0.0;
                 for (int c = 0; c < LO_D; ++c) s += (double)qv[c] * lo_bf16_to_f64(kp[i * LO_D + c]);
                 logit[p * LO_PAGE + i] = s / sqrt((double)LO_D);
@@ -525,10 +543,9 @@ void lo_attend(int batch, int hq, int hkv, int max_pages, const float* q, const 
             }
         }
         double z = 0.0;
-        for (int p = 0; p < n; ++p) {
-            int64_t phys = page_table[(int64_t)b * max_pages + sel[p]];
-            const uint16_t* vp = v_cache + (phys * hkv + kvh) * LO_PAGE * LO_D;
-            for (int i = 0; i < LO_PAGE; ++i) {
+        for (int p = 0; p < npages; ++p) {
+            const uint16_t* vp = v_cache + (phys[p] * hkv + kvh) * LO_PAGE * LO_D;
+            for (int i = 0; i < ntok[p]; ++i) {
                 double w = exp(logit[p * LO_PAGE + i] - mx);
                 z += w;
                 for (int c = 0; c < LO_D; ++c) o[c] += w * lo_bf16_to_f64(vp[i * LO_D + c]);
@@ -537,6 +554,8 @@ void lo_attend(int batch, int hq, int hkv, int max_pages, const float* q, const 
         for (int c = 0; c < LO_D; ++c) o[c] /= z;
         if (lse) lse[bh] = mx + log(z);
         free(logit);
+        free(ntok);
+        free(phys);
     }
 }
 

@@ -366,6 +366,43 @@ def test_attention_all_pages_is_dense_softmax(oracle_lib):
     assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
 
 
+def test_attention_tail_page(oracle_lib):
+    """The unfilled page (no summary yet) is attended whole: its first t tokens join the
+    selected pages' tokens in one softmax. Pinned against textbook softmax attention over
+    that token set; t = 16 equals selecting that page; t = 0 is no tail; an empty
+    selection with a tail attends the tail alone."""
+    rng = np.random.default_rng(51)
+    B, Hq, Hkv, P = 3, 4, 2, 6
+    kc = synth.f32_to_bf16_bits(rng.standard_normal((B * P, Hkv, 16, 128)).astype(np.float32))
+    vc = synth.f32_to_bf16_bits(rng.standard_normal((B * P, Hkv, 16, 128)).astype(np.float32))
+    q = rng.standard_normal((B, Hq, 128)).astype(np.float32)
+    table = rng.permutation(B * P).reshape(B, P).astype(np.int32)
+    seq = np.array([4, 5, 2], np.int32)          # full pages; the unfilled page is logical page seq[b]
+    tail = np.array([7, 16, 1], np.int32)
+    sel = np.zeros((B, Hkv, 2), np.int32)
+    sel[:, :, 0], sel[:, :, 1] = 0, 1
+    nsel = np.array([[2, 1], [2, 0], [1, 2]], np.int32)
+    out, lse = oracle_lib.attend(q, kc, vc, table, sel, nsel, seq, tail)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // 2
+            pages = [table[b, sel[b, kvh, i]] for i in range(nsel[b, kvh])]
+            kb = [kc[p_, kvh] for p_ in pages] + [kc[table[b, seq[b]], kvh][:tail[b]]]
+            vb = [vc[p_, kvh] for p_ in pages] + [vc[table[b, seq[b]], kvh][:tail[b]]]
+            o, l = _dense_attention(q[b, h], np.concatenate(kb), np.concatenate(vb))
+            assert np.allclose(out[b, h], o, atol=1e-12) and abs(lse[b, h] - l) < 1e-12
+    # t = 16 on page seq[1] = selecting that page as well
+    sel3 = np.concatenate([sel, np.full((B, Hkv, 1), 5, np.int32)], axis=2)
+    for kvh in range(Hkv):
+        sel3[1, kvh, nsel[1, kvh]] = seq[1]
+    out3, lse3 = oracle_lib.attend(q, kc, vc, table, sel3, nsel + np.array([[0, 0], [1, 1], [0, 0]], np.int32))
+    assert np.allclose(out3[1], out[1], atol=1e-12) and np.allclose(lse3[1], lse[1], atol=1e-12)
+    # t = 0: the plain selection
+    out0, lse0 = oracle_lib.attend(q, kc, vc, table, sel, nsel, seq, np.zeros(B, np.int32))
+    outn, lsen = oracle_lib.attend(q, kc, vc, table, sel, nsel)
+    assert np.array_equal(out0, outn) and np.array_equal(lse0, lsen)
+
+
 # -------------------------------------------------- whole step, carriers (P10)
 
 def test_tiny_workload_keeps_carriers(oracle_lib):
