@@ -242,8 +242,9 @@ def select(keys: np.ndarray, seq_pages, budget_tokens: int, k_cap: Optional[int]
 # ---------------------------------------------------------------- attention
 
 def attend(q, k_cache, v_cache, page_table, selected, n_selected, seq_pages=None, tail_tokens=None):
-    """(out [B][Hq][128] float64, lse [B][Hq]) over the selected pages, plus the first
-    tail_tokens[b] tokens of logical page seq_pages[b] (the unfilled page) when given."""
+    """(out [B][Hq][128] float64, lse [B][Hq]) over the selected pages, plus, when given,
+    the tail_tokens[b] tokens without a summary yet: logical pages seq_pages[b],
+    seq_pages[b] + 1, ... (16 tokens each, the last one partial)."""
     q = _c(q, np.float32)
     B, Hq, _ = q.shape
     kc, vc = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
@@ -266,7 +267,7 @@ def attend(q, k_cache, v_cache, page_table, selected, n_selected, seq_pages=None
 def decode_step(q, k_cache, v_cache, page_table, seq_pages, mu, basis, coef, scales, budget_tokens: int,
                 tail_tokens=None):
     """The whole step in float64: scores -> group keys -> select -> attend (plus the
-    unfilled page's tail_tokens tokens, attended whole, when given)."""
+    tail_tokens tokens without a summary, attended whole, when given)."""
     Hkv = k_cache.shape[1]
     s = scores(q, mu, basis, coef, scales, page_table, seq_pages, Hkv)
     keys, lse_h = group_keys(s, seq_pages, Hkv)

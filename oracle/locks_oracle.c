@@ -488,11 +488,13 @@ void lo_select(int batch, int hkv, int max_pages, const double* keys, const int3
 /*
  * Attention over the selected pages [p1 "Code": scaled dot-product attention of
  * q over the gathered keys/values of the chosen pages, default scale 1/sqrt(d)],
- * plus, when tail_tokens is given, the first tail_tokens[b] tokens of the
- * sequence's partially filled page (logical page seq_pages[b]). A page gets its
- * summary only once it fills [p1 "How LOCKS works": the decomposition runs when
- * a page fills, every 16 tokens], so the unfilled page cannot be scored; it is
- * attended whole (the pages are silent on it; this is the plain reading).
+ * plus, when tail_tokens is given, the sequence's tail_tokens[b] tokens that
+ * have no summary yet: logical pages seq_pages[b], seq_pages[b] + 1, ... (16
+ * tokens each, the last one partial). A page gets its summary only once it fills
+ * [p1 "How LOCKS works": the decomposition runs when a page fills, every 16
+ * tokens, off the decode critical path], so the page being filled, and a filled
+ * page whose summary is still being built, cannot be scored; they are attended
+ * whole (the pages are silent on them; this is the plain reading).
  * For every (b, query head h) with kv head h / g, over that token set:
  *   l_i = q . k_i / sqrt(128),  out = sum_i softmax(l)_i v_i,  lse = log sum_i exp(l_i).
  * An empty set gives out = 0 and lse = -inf.
@@ -519,17 +521,18 @@ void lo_attend(int batch, int hq, int hkv, int max_pages, const float* q, const 
             if (lse) lse[bh] = -INFINITY;
             continue;
         }
-        /* the token set: (physical page, tokens used) for each selected page, then the tail */
-        int npages = n + (tail > 0 ? 1 : 0);
+        /* the token set: (physical page, tokens used) for each selected page, then the tail pages */
+        int ntail = (tail + LO_PAGE - 1) / LO_PAGE;
+        int npages = n + ntail;
         int64_t* phys = (int64_t*)malloc(sizeof(int64_t) * npages);
         int* ntok = (int*)malloc(sizeof(int) * npages);
         for (int p = 0; p < n; ++p) {
             phys[p] = page_table[(int64_t)b * max_pages + sel[p]];
             ntok[p] = LO_PAGE;
         }
-        if (tail > 0) {
-            phys[n] = page_table[(int64_t)b * max_pages + seq_pages[b]];
-            ntok[n] = tail;
+        for (int j = 0; j < ntail; ++j) {
+            phys[n + j] = page_table[(int64_t)b * max_pages + seq_pages[b] + j];
+            ntok[n + j] = tail - j * LO_PAGE < LO_PAGE ? tail - j * LO_PAGE : LO_PAGE;
         }
         double* logit = (double*)malloc(sizeof(double) * npages * LO_PAGE);
         double mx = -INFINITY;

@@ -367,10 +367,11 @@ def test_attention_all_pages_is_dense_softmax(oracle_lib):
 
 
 def test_attention_tail_page(oracle_lib):
-    """The unfilled page (no summary yet) is attended whole: its first t tokens join the
+    """Tokens without a summary yet (the page being filled, and filled pages whose
+    summaries are still being built) are attended whole: the tail's t tokens join the
     selected pages' tokens in one softmax. Pinned against textbook softmax attention over
-    that token set; t = 16 equals selecting that page; t = 0 is no tail; an empty
-    selection with a tail attends the tail alone."""
+    that token set; t = 16 equals selecting that page; t = 0 is no tail; tails spanning
+    several pages."""
     rng = np.random.default_rng(51)
     B, Hq, Hkv, P = 3, 4, 2, 6
     kc = synth.f32_to_bf16_bits(rng.standard_normal((B * P, Hkv, 16, 128)).astype(np.float32))
@@ -401,6 +402,23 @@ def test_attention_tail_page(oracle_lib):
     out0, lse0 = oracle_lib.attend(q, kc, vc, table, sel, nsel, seq, np.zeros(B, np.int32))
     outn, lsen = oracle_lib.attend(q, kc, vc, table, sel, nsel)
     assert np.array_equal(out0, outn) and np.array_equal(lse0, lsen)
+    # a tail over several pages (filled pages whose summaries are not built yet, then a
+    # partial one): textbook softmax over the selected pages' tokens and those tokens
+    seq2 = np.array([1, 2, 0], np.int32)
+    tail2 = np.array([16 + 5, 32, 48 + 16], np.int32)
+    out2, lse2 = oracle_lib.attend(q, kc, vc, table, sel, nsel, seq2, tail2)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // 2
+            pages = [table[b, sel[b, kvh, i]] for i in range(nsel[b, kvh])]
+            kb = [kc[p_, kvh] for p_ in pages]
+            vb = [vc[p_, kvh] for p_ in pages]
+            for j in range((tail2[b] + 15) // 16):
+                nt = min(16, tail2[b] - 16 * j)
+                kb.append(kc[table[b, seq2[b] + j], kvh][:nt])
+                vb.append(vc[table[b, seq2[b] + j], kvh][:nt])
+            o, l = _dense_attention(q[b, h], np.concatenate(kb), np.concatenate(vb))
+            assert np.allclose(out2[b, h], o, atol=1e-12) and abs(lse2[b, h] - l) < 1e-12
 
 
 # -------------------------------------------------- whole step, carriers (P10)
