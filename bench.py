@@ -455,6 +455,54 @@ def run_locks(args, rank, world, local):
                                "can stay in L2 for the next, which separate layers' caches would not"}
         assert L.locks_get_device_status(ws) == 0, "device status after the model graph"
 
+    # page-fill refresh (outside the timed region): the one-page summary build a filled page
+    # needs, alone and overlapped with a decode step on a second stream
+    refresh = None
+    if not args.no_model_graph:
+        side = torch.cuda.Stream()
+        one = ids[:1].clone()                                        # physical page 0
+        fresh = L.Summaries.empty(1, w.num_kv_heads, dev)            # its new summary (not read by the step)
+        L.locks_build_summaries(dims, kc, one, 1, fresh)
+        torch.cuda.synchronize()
+        alone, with_refresh, plain = [], [], []
+        for i in range(12):
+            flush.zero_()
+            torch.cuda.synchronize()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(side)
+            L.locks_build_summaries(dims, kc, one, 1, fresh, stream=side)
+            b_.record(side)
+            torch.cuda.synchronize()
+            # three consecutive steps, then the same with the one-page build launched on the
+            # second stream right after the first step's kernels are queued
+            for with_build, acc in ((False, plain), (True, with_refresh)):
+                flush.zero_()
+                torch.cuda.synchronize()
+                c_, d_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c_.record(stream)
+                for k in range(3):
+                    g_score.replay()
+                    g_sa.replay()
+                    if with_build and k == 0:
+                        side.wait_stream(stream)
+                        with torch.cuda.stream(side):
+                            L.locks_build_summaries(dims, kc, one, 1, fresh, stream=side)
+                d_.record(stream)
+                torch.cuda.synchronize()
+                if i >= 2:
+                    acc.append(c_.elapsed_time(d_) * 1000.0)
+            if i >= 2:
+                alone.append(a_.elapsed_time(b_) * 1000.0)
+        refresh = {"build_one_page_us": statistics.mean(alone), "three_steps_us": statistics.mean(plain),
+                   "three_steps_with_refresh_us": statistics.mean(with_refresh),
+                   "refresh_cost_us": statistics.mean(with_refresh) - statistics.mean(plain),
+                   "samples": len(alone),
+                   "path": "locks_build_summaries(n_pages=1) for a page that just filled, on a second stream, "
+                           "launched after the first of three consecutive steps is queued (the page stays in "
+                           "the tail, attended whole, until the build completes); refresh_cost_us = the "
+                           "three steps' extra time"}
+        assert L.locks_get_device_status(ws) == 0, "device status after the refresh timing"
+
     # dense comparator (outside the timed region): the same attention kernel with every page
     # of every sequence selected, i.e. exact attention over the whole cache
     dense = None
@@ -519,6 +567,7 @@ def run_locks(args, rank, world, local):
         "bytes_vs_dense": (w.batch * w.pages * w.num_kv_heads * PAGE_KV_BYTES) / step_bytes,
         "dense_comparator": dense,
         "model_graph": model_graph,
+        "page_refresh": refresh,
         "roofline": {"kernel": "score_pages (locks_score_pages)", "bound": "hbm", "achieved": score_gbs,
                      "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": score_gbs / hbm,

@@ -87,6 +87,7 @@ extern "C" {
 
 #define LOCKS_HEAD_DIM 128
 #define LOCKS_PAGE_SIZE 16
+#define LOCKS_MAX_TAIL_PAGES 4  /* pages without a summary that one tail may span */
 #define LOCKS_RANK 8
 #define LOCKS_MAX_GROUP 16
 #define LOCKS_UNIT_BYTES 776
@@ -235,6 +236,37 @@ LOCKS_API int locks_decode_step(const locks_dims_t* dims, const float* q, const 
                                 const int32_t* page_table, const int32_t* seq_pages, int32_t budget_tokens,
                                 uint16_t* out, float* lse, float* scores, int32_t* selected,
                                 int32_t* n_selected, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * As locks_select_attend and locks_decode_step, plus each sequence's tokens that
+ * have no summary yet. A page gets its summary only once it fills (LOCKS post,
+ * "How LOCKS works": the decomposition runs when a page fills, every 16 tokens,
+ * off the decode critical path), so the page being filled, and a filled page
+ * whose summary is still being built, cannot be scored; their tokens are
+ * attended whole, in the same softmax as the selected pages, and never selected.
+ *   tail_tokens  int32 [batch], may be NULL (no tail): tail_tokens[b] in
+ *                [0, 16 * LOCKS_MAX_TAIL_PAGES] tokens on logical pages
+ *                seq_pages[b], seq_pages[b] + 1, ... (16 per page, the last one
+ *                partial; physical pages through page_table, so the tail must end
+ *                within max_pages_per_seq); other values record
+ *                LOCKS_ERR_BAD_INDEX and the tail is skipped.
+ * Page-fill refresh: when a page fills, the caller launches locks_build_summaries
+ * for it (n_pages = 1) on another stream and keeps its 16 tokens in the tail
+ * until that build has completed; then it advances seq_pages[b] by one and
+ * takes 16 off tail_tokens[b].
+ */
+LOCKS_API int locks_select_attend_tail(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                       const uint16_t* v_cache, const int32_t* page_table, const float* scores,
+                                       const float* lse_partials, const int32_t* seq_pages,
+                                       const int32_t* tail_tokens, int32_t budget_tokens, int32_t* selected,
+                                       int32_t* n_selected, uint16_t* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+LOCKS_API int locks_decode_step_tail(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                     const uint16_t* v_cache, locks_summaries_t summaries,
+                                     const int32_t* page_table, const int32_t* seq_pages,
+                                     const int32_t* tail_tokens, int32_t budget_tokens, uint16_t* out, float* lse,
+                                     float* scores, int32_t* selected, int32_t* n_selected, void* workspace,
+                                     size_t workspace_bytes, void* stream);
 
 /*
  * locks_decode_step without a workspace (the LOCKS pages have no counterpart

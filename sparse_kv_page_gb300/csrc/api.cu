@@ -177,7 +177,7 @@ locks::SelectAttendArgs sa_args(const locks_dims_t* dims, void* ws) {
 
 int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
                        const int32_t* page_table, const float* scores, const float* partials,
-                       const int32_t* seq_pages,
+                       const int32_t* seq_pages, const int32_t* tail_tokens,
                        int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
                        void* workspace, cudaStream_t st) {
     const int dev = current_device();
@@ -195,6 +195,7 @@ int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t*
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.page_table = page_table;
+    a.tail_tokens = tail_tokens;
     a.out = out;
     a.lse = lse;
     const int cl = cluster_size(dev, dims, locks::SAMode::kSelectAttend);
@@ -335,6 +336,16 @@ int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t
                         const int32_t* page_table, const float* scores, const float* lse_partials,
                         const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected, int32_t* n_selected,
                         uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    return locks_select_attend_tail(dims, q, k_cache, v_cache, page_table, scores, lse_partials, seq_pages, nullptr,
+                                    budget_tokens, selected, n_selected, out, lse, workspace, workspace_bytes,
+                                    stream);
+}
+
+int locks_select_attend_tail(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                             const uint16_t* v_cache, const int32_t* page_table, const float* scores,
+                             const float* lse_partials, const int32_t* seq_pages, const int32_t* tail_tokens,
+                             int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out,
+                             float* lse, void* workspace, size_t workspace_bytes, void* stream) {
     int v = validate_dims(dims);
     if (v != LOCKS_OK) return v;
     if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
@@ -344,7 +355,7 @@ int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t
     if (!aligned(q, 8) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return LOCKS_ERR_INVALID_ARG;
     if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
     if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelectAttend)) return LOCKS_ERR_UNSUPPORTED;
-    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, lse_partials, seq_pages,
+    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, lse_partials, seq_pages, tail_tokens,
                               budget_tokens, selected, n_selected, out, lse, workspace,
                               static_cast<cudaStream_t>(stream));
 }
@@ -353,6 +364,16 @@ int locks_decode_step(const locks_dims_t* dims, const float* q, const uint16_t* 
                       locks_summaries_t summaries, const int32_t* page_table, const int32_t* seq_pages,
                       int32_t budget_tokens, uint16_t* out, float* lse, float* scores, int32_t* selected,
                       int32_t* n_selected, void* workspace, size_t workspace_bytes, void* stream) {
+    return locks_decode_step_tail(dims, q, k_cache, v_cache, summaries, page_table, seq_pages, nullptr,
+                                  budget_tokens, out, lse, scores, selected, n_selected, workspace, workspace_bytes,
+                                  stream);
+}
+
+int locks_decode_step_tail(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                           const uint16_t* v_cache, locks_summaries_t summaries, const int32_t* page_table,
+                           const int32_t* seq_pages, const int32_t* tail_tokens, int32_t budget_tokens,
+                           uint16_t* out, float* lse, float* scores, int32_t* selected, int32_t* n_selected,
+                           void* workspace, size_t workspace_bytes, void* stream) {
     int v = validate_dims(dims);
     if (v != LOCKS_OK) return v;
     if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
@@ -373,8 +394,8 @@ int locks_decode_step(const locks_dims_t* dims, const float* q, const uint16_t* 
         v = score_impl(dims, q, summaries, page_table, seq_pages, scores, partials, workspace, st);
         if (v != LOCKS_OK) return v;
     }
-    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, partials, seq_pages, budget_tokens,
-                              selected, n_selected, out, lse, workspace, st);
+    return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, partials, seq_pages, tail_tokens,
+                              budget_tokens, selected, n_selected, out, lse, workspace, st);
 }
 
 int locks_get_device_status(const void* workspace, int32_t* status, void* stream) {

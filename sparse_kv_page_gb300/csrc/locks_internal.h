@@ -64,6 +64,7 @@ struct SelectAttendArgs {
     const uint16_t* k_cache;
     const uint16_t* v_cache;
     const int32_t* page_table;
+    const int32_t* tail_tokens;   // nullable: tokens of each sequence's unfilled page (fused mode)
     uint16_t* out;
     float* lse;               // nullable
     int batch, hq, hkv, max_pages, num_phys;

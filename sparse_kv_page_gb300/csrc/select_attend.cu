@@ -550,9 +550,24 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, t = lane & 3;
     const int g = a.hq / a.hkv;
-    const int per = (n_sel + CL - 1) / CL;
-    const int p0 = min(n_sel, static_cast<int>(rank) * per);
-    const int p1 = min(n_sel, p0 + per);
+    bool failed = false, bad = false;
+    // the sequence's tokens without a summary yet (fused mode): `tail` tokens on logical
+    // pages tail_page, tail_page + 1, ... after the selected ones, attended whole
+    int tail = 0, tail_page = 0;
+    if (a.tail_tokens) {
+        tail = a.tail_tokens[b];
+        tail_page = a.seq_pages[b];
+        const int npg = (tail + kPage - 1) / kPage;
+        if (tail < 0 || tail > kPage * LOCKS_MAX_TAIL_PAGES ||
+            (tail > 0 && (tail_page < 0 || tail_page + npg > a.max_pages))) {
+            bad = true;
+            tail = 0;
+        }
+    }
+    const int n_all = n_sel + (tail + kPage - 1) / kPage;
+    const int per = (n_all + CL - 1) / CL;
+    const int p0 = min(n_all, static_cast<int>(rank) * per);
+    const int p1 = min(n_all, p0 + per);
 
     if (!q_staged) {
         float qv[16 * kD / kThreads];
@@ -569,9 +584,10 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     uint8_t* slot = ring + warp * kPageSlotBytes;
     uint64_t* bar = &sh.bar[warp];
     uint32_t phase = 0;
-    bool failed = false, bad = false;
     for (int p = p0 + warp; p < p1; p += kWarps) {
-        int logical = sel_coherent ? __ldcg(sel + p) : sel[p];
+        // tokens of the page that are attended
+        const int valid = p < n_sel ? kPage : min(kPage, tail - (p - n_sel) * kPage);
+        int logical = p < n_sel ? (sel_coherent ? __ldcg(sel + p) : sel[p]) : tail_page + (p - n_sel);
         if (logical < 0 || logical >= a.max_pages) {
             bad = true;
             logical = 0;
@@ -611,6 +627,22 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             mma_bf16_16816(sacc[0], ql, kb[0], kb[1]);
             mma_bf16_16816(sacc[1], qh, kb[2], kb[3]);
             mma_bf16_16816(sacc[1], ql, kb[2], kb[3]);
+        }
+        if (valid < kPage) {
+            // the unfilled page: tokens >= valid take no part (logits -inf; their V rows,
+            // which need not hold finite values, are zeroed before P V)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tok = nt * 8 + 2 * t;
+                if (tok >= valid) sacc[nt][0] = sacc[nt][2] = -INFINITY;
+                if (tok + 1 >= valid) sacc[nt][1] = sacc[nt][3] = -INFINITY;
+            }
+            for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
+                const int r = valid + (idx >> 4), box = (idx >> 3) & 1, c = idx & 7;
+                *reinterpret_cast<uint4*>(const_cast<uint8_t*>(vslot) + box * kBoxBytes + r * 128 + c * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
         }
         // online softmax (log2 domain); rows gid (c0, c1) and gid + 8 (c2, c3)
         float mx_a = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));

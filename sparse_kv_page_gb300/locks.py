@@ -83,6 +83,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             "locks_sparse_attention": ([D, P, P, P, P, P, P, I32, P, P, P, S, P], ctypes.c_int),
             "locks_select_attend": ([D, P, P, P, P, P, P, P, I32, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_decode_step": ([D, P, P, P, SUM, P, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_select_attend_tail": ([D, P, P, P, P, P, P, P, P, I32, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_decode_step_tail": ([D, P, P, P, SUM, P, P, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_get_device_status": ([P, ctypes.POINTER(I32), P], ctypes.c_int),
             "locks_clear_device_status": ([P, P], ctypes.c_int),
             "locks_set_wait_limit_ns": ([U64], ctypes.c_int),
@@ -220,21 +222,39 @@ def locks_sparse_attention(dims, q, k_cache, v_cache, page_table, selected, n_se
 
 
 def locks_select_attend(dims, q, k_cache, v_cache, page_table, scores, seq_pages, budget_tokens, selected,
-                        n_selected, out, lse=None, workspace=None, stream=None, lse_partials=None) -> None:
+                        n_selected, out, lse=None, workspace=None, stream=None, lse_partials=None,
+                        tail_tokens=None) -> None:
+    """tail_tokens (int32 [batch], optional): tokens of each sequence's unfilled page
+    (logical page seq_pages[b]), attended whole (locks_select_attend_tail)."""
     ws, nws = _ws(workspace)
-    _check("locks_select_attend", load_library().locks_select_attend(
-        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(scores),
-        _ptr(lse_partials), _ptr(seq_pages), int(budget_tokens), _ptr(selected), _ptr(n_selected), _ptr(out),
-        _ptr(lse), ws, nws, _stream(stream)))
+    if tail_tokens is None:
+        _check("locks_select_attend", load_library().locks_select_attend(
+            ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(scores),
+            _ptr(lse_partials), _ptr(seq_pages), int(budget_tokens), _ptr(selected), _ptr(n_selected), _ptr(out),
+            _ptr(lse), ws, nws, _stream(stream)))
+    else:
+        _check("locks_select_attend_tail", load_library().locks_select_attend_tail(
+            ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(scores),
+            _ptr(lse_partials), _ptr(seq_pages), _ptr(tail_tokens), int(budget_tokens), _ptr(selected),
+            _ptr(n_selected), _ptr(out), _ptr(lse), ws, nws, _stream(stream)))
 
 
 def locks_decode_step(dims, q, k_cache, v_cache, summaries: Summaries, page_table, seq_pages, budget_tokens, out,
-                      workspace, lse=None, scores=None, selected=None, n_selected=None, stream=None) -> None:
+                      workspace, lse=None, scores=None, selected=None, n_selected=None, stream=None,
+                      tail_tokens=None) -> None:
+    """tail_tokens (int32 [batch], optional): tokens of each sequence's unfilled page
+    (logical page seq_pages[b]), attended whole (locks_decode_step_tail)."""
     ws, nws = _ws(workspace)
-    _check("locks_decode_step", load_library().locks_decode_step(
-        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), summaries.c(), _ptr(page_table),
-        _ptr(seq_pages), int(budget_tokens), _ptr(out), _ptr(lse), _ptr(scores), _ptr(selected),
-        _ptr(n_selected), ws, nws, _stream(stream)))
+    if tail_tokens is None:
+        _check("locks_decode_step", load_library().locks_decode_step(
+            ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), summaries.c(), _ptr(page_table),
+            _ptr(seq_pages), int(budget_tokens), _ptr(out), _ptr(lse), _ptr(scores), _ptr(selected),
+            _ptr(n_selected), ws, nws, _stream(stream)))
+    else:
+        _check("locks_decode_step_tail", load_library().locks_decode_step_tail(
+            ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), summaries.c(), _ptr(page_table),
+            _ptr(seq_pages), _ptr(tail_tokens), int(budget_tokens), _ptr(out), _ptr(lse), _ptr(scores),
+            _ptr(selected), _ptr(n_selected), ws, nws, _stream(stream)))
 
 
 def locks_get_device_status(workspace, stream=None) -> int:
