@@ -12,8 +12,8 @@
 //    into a 4-stage shared-memory ring with bulk async copies (TMA engine,
 //    L2 evict-first) plus 8-byte LDGSTS for the fp16 scales, completion on
 //    mbarriers; a group of 8 consumer warps takes a stage, each warp one kv
-//    head and 8 pages; two groups work on alternate stages (one group when
-//    the GQA group is > 8, whose register footprint allows only one).
+//    head and 8 pages; two groups work on alternate stages, or, when the GQA
+//    group is > 8, both on every stage with 8 of its query heads each.
 //  * V^T q and mu . q run on the tensor cores (mma.sync m16n8k16, f16 in,
 //    fp32 accumulate): A = the codes plus their offset (int4 + 8, int8 + 128),
 //    read directly as f16 subnormals u * 2^-24 by masking (no conversion
@@ -46,6 +46,8 @@ __device__ __forceinline__ float pow2i(int e) {  // 2^e for |e| <= 126
     return __int_as_float((127 + e) << 23);
 }
 
+// Two consumer groups for NT <= 2. HS = 1: they take alternate stages. HS = 2
+// (GQA group 16): both take every stage, group i computing heads 8i .. 8i + 7.
 template <int NT>
 struct Shape {
     static constexpr int kGroups = NT <= 2 ? 2 : 1;
@@ -53,7 +55,7 @@ struct Shape {
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
 };
 
-template <int HKV, int NT>
+template <int HKV, int NT, int HS>
 __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs a, int nchunks, int total_items) {
     constexpr int NP = kStageUnits / HKV;   // pages per stage
     constexpr int kGroups = Shape<NT>::kGroups;
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 33);              // 1 expect_tx arrive + 32 LDGSTS arrives
-            mbar_init(&empty[s], kGroupWarps);
+            mbar_init(&empty[s], HS == 2 ? kConsumerWarps : kGroupWarps);
         }
         fence_barrier_init();
     }
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
         const int kvh = gw % HKV, blk = gw / HKV;
         const int gid = lane >> 2, t = lane & 3;
         const int g = a.hq / HKV;
+        const int hoff = HS == 2 ? group * 4 * NT : 0;   // first head (within the kv group) of this group
         uint32_t bq[8][NT][2];
         float qsum[NT];    // sum of that head's pre-scaled query q' (code-offset correction)
         float qsc[NT];     // 2^e of the output head (4 nt + t) of this thread
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
             }
             const int nvalid = min(NP, cur_P - page0);
             if (nvalid <= 0) continue;
-            if (static_cast<int>(k % kGroups) != group) {   // the other group's stage
+            if (HS == 1 && static_cast<int>(k % kGroups) != group) {   // the other group's stage
                 ++k;
                 continue;
             }
@@ -189,9 +192,9 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
 #pragma unroll
                 for (int hh = 0; hh < 4 * NT; ++hh) {
                     float mx = 0.f, sm = 0.f;
-                    if (hh < g) {
+                    if (hoff + hh < g) {
                         const float4 v = *reinterpret_cast<const float4*>(
-                            a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * kD + lane * 4);
+                            a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hoff + hh) * kD + lane * 4);
                         mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
                         sm = (v.x + v.y) + (v.z + v.w);
                     }
@@ -217,11 +220,11 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                     qsc[nt] = pow2i(eO[nt]);
                     const int col = nt * 8 + gid, hh = col >> 1, hl = col & 1;
                     const float inv = pow2i(-eB[nt]);
-                    const float* qrow = a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * kD;
+                    const float* qrow = a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + hoff + hh) * kD;
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         uint32_t r0 = 0, r1 = 0;
-                        if (hh < g) {
+                        if (hoff + hh < g) {
                             const float2 x01 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t);
                             const float2 x89 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t + 8);
                             const uint32_t p0 = split_f16_hilo(x01.x * inv), p1 = split_f16_hilo(x01.y * inv);
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                         z += __shfl_xor_sync(0xffffffffu, z, 4);
                         z += __shfl_xor_sync(0xffffffffu, z, 8);
                         z += __shfl_xor_sync(0xffffffffu, z, 16);
-                        const int hh = 4 * nt + t;
+                        const int hh = hoff + 4 * nt + t;
                         if (gid == 0 && hh < g)
                             reinterpret_cast<float2*>(a.lse_partials)
                                 [(static_cast<int64_t>(b) * a.hq + kvh * g + hh) * nblk + blk8] = make_float2(m, z);
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                     const int page = page0 + 8 * blk + gid;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const int hh = 4 * nt + t;
+                        const int hh = hoff + 4 * nt + t;
                         if (hh < g)
                             a.scores[(static_cast<int64_t>(b) * a.hq + kvh * g + hh) * a.max_pages + page] =
                                 score_out[nt];
@@ -419,25 +422,25 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
     if (failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
 }
 
-template <int HKV, int NT>
+template <int HKV, int NT, int HS>
 cudaError_t launch_t(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
     constexpr int NP = kStageUnits / HKV;
     const int nchunks = (a.max_pages + NP - 1) / NP;
     const int total = a.batch * nchunks;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = ensure_kernel_attrs<score_kernel<HKV, NT>>(kSmemBytes);
+    cudaError_t e = ensure_kernel_attrs<score_kernel<HKV, NT, HS>>(kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = min(total, num_sms);
-    score_kernel<HKV, NT><<<grid, Shape<NT>::kThreads, kSmemBytes, stream>>>(a, nchunks, total);
+    score_kernel<HKV, NT, HS><<<grid, Shape<NT>::kThreads, kSmemBytes, stream>>>(a, nchunks, total);
     return cudaGetLastError();
 }
 
 template <int HKV>
 cudaError_t launch_h(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
     const int g = a.hq / a.hkv;
-    if (g <= 4) return launch_t<HKV, 1>(a, num_sms, stream);
-    if (g <= 8) return launch_t<HKV, 2>(a, num_sms, stream);
-    return launch_t<HKV, 4>(a, num_sms, stream);
+    if (g <= 4) return launch_t<HKV, 1, 1>(a, num_sms, stream);
+    if (g <= 8) return launch_t<HKV, 2, 1>(a, num_sms, stream);
+    return launch_t<HKV, 2, 2>(a, num_sms, stream);   // g = 9..16: the two groups split the heads
 }
 
 }  // namespace
