@@ -3,9 +3,11 @@ bench.py times (grid, cluster size and stage split follow the full dims).
 
 The summaries are random valid bytes (every code in range) so no K is needed to
 score; the oracle scores the same bytes in float64 over the whole table and makes
-its own selection from its own scores. K and V are then filled (seeded) only on
-the pages the GPU selected, the full fused decode step runs, and the oracle
-attends over the same pages from a compacted copy of them.
+its own selection from its own scores. The key and selection stage is also run on
+one seeded score table given to both sides. K and V are then filled (seeded) only
+on the pages the oracle selected, the fused decode step runs, and the oracle
+attends over its selection from a compacted copy of those pages. Nothing the GPU
+computes is given to the oracle.
 """
 import numpy as np
 import pytest
@@ -20,16 +22,18 @@ pytestmark = pytest.mark.gpu
 from tests.gpu_util import DEV, bf16_out, check_selection, cosine, t, upload_summaries  # noqa: E402
 
 SCORE_TOL = 1e-3
-KEY_TOL_S2 = 2e-4   # fp32 log-sum-exp over up to 65,536 pages, hardware exp2/log2
-KEY_TOL = 2e-3      # plus the scores' own error
+KEY_TOL_S2 = 2e-4   # same scores on both sides: fp32 log-sum-exp over up to 65,536 pages
+KEY_TOL = 2e-3      # each side's keys from its own scores: plus the scores' error
 ATT_ABS = 2e-2
 ATT_COS = 0.9995
 
 
-@pytest.mark.parametrize("wname", ["llama8b_128k", "batch8_256k", "ctx1m", "glm9b_4x1m"])
-def test_full_size_decode_step(wname):
+CASES = [(n, b) for n in ("llama8b_128k", "batch8_256k", "ctx1m", "glm9b_4x1m") for b in synth.WORKLOADS[n].budgets]
+
+
+@pytest.mark.parametrize("wname,budget", CASES)
+def test_full_size_decode_step(wname, budget):
     w = synth.WORKLOADS[wname]
-    budget = max(w.budgets)
     B, Hq, Hkv, P, nphys = w.batch, w.num_q_heads, w.num_kv_heads, w.pages, w.num_phys_pages
     q = synth.make_queries(w)
     table = synth.make_page_table(w)
@@ -43,12 +47,13 @@ def test_full_size_decode_step(wname):
     # 1. scores (with the LSE partials, as in the decode step) against the oracle's full table
     scores = torch.empty((B, Hq, P), dtype=torch.float32, device=DEV)
     part = torch.empty(L.lse_partials_shape(dims), dtype=torch.float32, device=DEV)
-    L.locks_score_pages(dims, qd, summ, td, sd, scores, ws, lse_partials=part)
+    L.locks_score_pages(dims, qd, summ, td, sd, scores, workspace=ws, lse_partials=part)
     torch.cuda.synchronize()
     ref_s = oracle.scores(q, summ_np.mu, summ_np.basis, summ_np.coef, summ_np.scales, table, seq, Hkv)
     assert np.abs(scores.cpu().numpy() - ref_s).max() < SCORE_TOL
 
-    # 2. selection: the oracle selects from its own scores
+    # 2. selection from those scores (with the partials, as the step does): the oracle
+    #    selects from its own scores, so pages may differ only at the k-th key
     keys, _ = oracle.group_keys(ref_s, seq, Hkv)
     osel, on = oracle.select(keys, seq, budget)
     k_cap = L.locks_k_cap(dims, budget)
@@ -60,21 +65,25 @@ def test_full_size_decode_step(wname):
     assert L.locks_get_device_status(ws) == 0
     sel_np, nsel_np = sel.cpu().numpy(), nsel.cpu().numpy()
     check_selection(sel_np, nsel_np, osel, on, keys, seq)
-    # the keys alone: against the oracle's keys of the GPU's own scores (S2 in isolation),
-    # then against the oracle's keys of its own scores (S1 and S2 together)
-    gk = gkeys.cpu().numpy()
-    own, _ = oracle.group_keys(scores.cpu().numpy(), seq, Hkv)
-    assert np.abs(gk - own).max() < KEY_TOL_S2
-    assert np.abs(gk - keys).max() < KEY_TOL
+    assert np.abs(gkeys.cpu().numpy() - keys).max() < KEY_TOL
 
-    # 3. the whole fused step; K/V exist only on the pages selected (seeded values)
-    rng = np.random.default_rng(w.seed_of(0) + 200)
+    # 3. the key and selection stage alone, on one seeded score table given to both sides
+    rng = np.random.default_rng(w.seed_of(0) + 300)
+    rs = (rng.standard_normal((B, Hq, P)) * 2.0).astype(np.float32)
+    rkeys, _ = oracle.group_keys(rs, seq, Hkv)
+    rsel, rn = oracle.select(rkeys, seq, budget)
+    L.locks_select_pages(dims, t(rs), sd, budget, sel, nsel, sel_keys=gkeys, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.abs(gkeys.cpu().numpy() - rkeys).max() < KEY_TOL_S2
+    check_selection(sel.cpu().numpy(), nsel.cpu().numpy(), rsel, rn, rkeys, seq, tol=KEY_TOL_S2)
+
+    # 4. the whole fused step; K/V exist only on the pages the oracle selected (seeded values)
     kc = torch.zeros((nphys, Hkv, 16, 128), dtype=torch.int16, device=DEV)
     vc = torch.zeros_like(kc)
     comp_table = np.zeros((B, P), np.int32)
     kparts, vparts, n_comp = [], [], 0
     for b in range(B):
-        pages = np.unique(sel_np[b][:, :k_cap][np.arange(k_cap)[None, :] < nsel_np[b][:, None]])
+        pages = np.unique(osel[b][np.arange(osel.shape[2])[None, :] < on[b][:, None]])
         kb = synth.f32_to_bf16_bits(rng.standard_normal((len(pages), Hkv, 16, 128)).astype(np.float32))
         vb = synth.f32_to_bf16_bits(rng.standard_normal((len(pages), Hkv, 16, 128)).astype(np.float32))
         phys = torch.from_numpy(table[b, pages].astype(np.int64)).to(DEV)
@@ -91,9 +100,15 @@ def test_full_size_decode_step(wname):
     L.locks_decode_step(dims, qd, kc, vc, summ, td, sd, budget, out, ws, lse=lse, selected=sel2, n_selected=nsel2)
     torch.cuda.synchronize()
     assert L.locks_get_device_status(ws) == 0
-    assert torch.equal(sel2, sel) and torch.equal(nsel2, nsel)
-    ref_o, ref_l = oracle.attend(q, np.concatenate(kparts), np.concatenate(vparts), comp_table, sel_np, nsel_np)
+    # the step's selection is the one the separate calls made in 2.
+    assert np.array_equal(sel2.cpu().numpy(), sel_np) and np.array_equal(nsel2.cpu().numpy(), nsel_np)
+    ref_o, ref_l = oracle.attend(q, np.concatenate(kparts), np.concatenate(vparts), comp_table, osel, on)
+    # outputs are compared on the (request, kv head) segments whose selection is the
+    # oracle's; others differ only at the boundary key, which 2. has verified
+    same = np.array([[np.array_equal(sel_np[b, h], osel[b, h]) for h in range(Hkv)] for b in range(B)])
+    assert same.mean() >= 0.75, same
+    heads = np.repeat(same, Hq // Hkv, axis=1)
     got = bf16_out(out)
-    assert np.abs(got - ref_o).max() < ATT_ABS
-    assert cosine(got, ref_o).min() >= ATT_COS
-    assert np.abs(lse.cpu().numpy() - ref_l).max() < 1e-3
+    assert np.abs(got - ref_o)[heads].max() < ATT_ABS
+    assert cosine(got, ref_o)[heads].min() >= ATT_COS
+    assert np.abs(lse.cpu().numpy() - ref_l)[heads].max() < 1e-3
