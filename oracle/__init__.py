@@ -15,6 +15,11 @@ ctypes. Each function cites the LOCKS page passage it follows:
 * group    - summary 2.3 (mean of the estimated mass shares of a GQA group)
 * select   - "Code": k = budget // 16 pages, indices sorted ascending
 * attend   - "Code": scaled dot-product attention over the selected pages
+* ablations - exact (read-all-keys) page scores (Korean gist.science summary,
+             sections 1 and 3); rank / bit-width variants of the summary
+             ("Caveats": int4 loses a few recall points, int2 collapses); a
+             shared basis and its projected scores ("Why shared-basis sparse
+             attention is structurally broken"; Proposition 1)
 
 Parity unpinned: nothing here is unpinned; see tests/test_oracle_pins.py for
 the checks that tie every function to the pages and to the mathematics.
@@ -78,6 +83,12 @@ def _load() -> ctypes.CDLL:
                 "lo_group_keys": ([i32, i32, i32, i32, P, P, P, P], None),
                 "lo_select": ([i32, i32, i32, P, P, i32, i32, P, P], None),
                 "lo_attend": ([i32, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P], None),
+                "lo_exact_score_unit": ([P, P], f64),
+                "lo_exact_scores": ([i32, i32, i32, i32, P, P, P, P, P], None),
+                "lo_quant_dequant": ([P, i32, i32], None),
+                "lo_variant_scores": ([i32, i32, i32, i32, P, P, P, P, i32, i32, i32, i32, P], None),
+                "lo_shared_basis": ([i32, i32, i32, P, P, P, i32, P, P], None),
+                "lo_shared_scores": ([i32, i32, i32, i32, P, P, P, P, P, i32, P], None),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -274,3 +285,67 @@ def decode_step(q, k_cache, v_cache, page_table, seq_pages, mu, basis, coef, sca
     sel, nsel = select(keys, seq_pages, budget_tokens)
     out, lse = attend(q, k_cache, v_cache, page_table, sel, nsel, seq_pages, tail_tokens)
     return dict(scores=s, keys=keys, head_lse=lse_h, selected=sel, n_selected=nsel, out=out, lse=lse)
+
+
+# --------------------------------------------------------------- ablations
+
+def _cache_args(q, k_cache, page_table, seq_pages):
+    q = _c(q, np.float32)
+    kc = _c(k_cache, np.uint16)
+    table = _c(page_table, np.int32)
+    return q, kc, table, _c(seq_pages, np.int32)
+
+
+def exact_score_unit(q, k_bits) -> float:
+    """log sum_i exp(q . k_i / sqrt(d)) over one page's 16 bf16 keys."""
+    return _load().lo_exact_score_unit(_p(_c(q, np.float64)), _p(_c(k_bits, np.uint16).reshape(PAGE, D)))
+
+
+def exact_scores(q, k_cache, page_table, seq_pages) -> np.ndarray:
+    """[B][Hq][max_pages] exact page scores from all keys (NaN where j >= seq_pages[b])."""
+    q, kc, table, seq = _cache_args(q, k_cache, page_table, seq_pages)
+    B, Hq, _ = q.shape
+    out = np.full((B, Hq, table.shape[1]), np.nan)
+    _load().lo_exact_scores(B, Hq, kc.shape[1], table.shape[1], _p(q), _p(kc), _p(table), _p(seq), _p(out))
+    return out
+
+
+def quant_dequant(x, bits: int) -> np.ndarray:
+    """x dequantised from its symmetric absmax codes of `bits` bits (0 = unchanged)."""
+    y = _c(x, np.float64).copy()
+    _load().lo_quant_dequant(_p(y), y.size, int(bits))
+    return y
+
+
+def variant_scores(q, k_cache, page_table, seq_pages, rank: int, bits_mu: int, bits_v: int,
+                   bits_c: int) -> np.ndarray:
+    """[B][Hq][max_pages] scores of rank-`rank` summaries quantised to the given widths."""
+    q, kc, table, seq = _cache_args(q, k_cache, page_table, seq_pages)
+    B, Hq, _ = q.shape
+    out = np.full((B, Hq, table.shape[1]), np.nan)
+    _load().lo_variant_scores(B, Hq, kc.shape[1], table.shape[1], _p(q), _p(kc), _p(table), _p(seq),
+                              int(rank), int(bits_mu), int(bits_v), int(bits_c), _p(out))
+    return out
+
+
+def shared_basis(k_cache, page_table, seq_pages, rank: int):
+    """(basis [B][Hkv][rank][128], eigvals [B][Hkv][128]) of each sequence's key second moment."""
+    kc = _c(k_cache, np.uint16)
+    table = _c(page_table, np.int32)
+    seq = _c(seq_pages, np.int32)
+    B, Hkv = table.shape[0], kc.shape[1]
+    basis = np.zeros((B, Hkv, rank, D))
+    ev = np.zeros((B, Hkv, D))
+    _load().lo_shared_basis(B, Hkv, table.shape[1], _p(kc), _p(table), _p(seq), int(rank), _p(basis), _p(ev))
+    return basis, ev
+
+
+def shared_scores(q, k_cache, page_table, seq_pages, basis) -> np.ndarray:
+    """[B][Hq][max_pages] scores of the keys projected on the shared basis ([B][Hkv][rank][128])."""
+    q, kc, table, seq = _cache_args(q, k_cache, page_table, seq_pages)
+    w = _c(basis, np.float64)
+    B, Hq, _ = q.shape
+    out = np.full((B, Hq, table.shape[1]), np.nan)
+    _load().lo_shared_scores(B, Hq, kc.shape[1], table.shape[1], _p(q), _p(kc), _p(table), _p(seq), _p(w),
+                             w.shape[2], _p(out))
+    return out

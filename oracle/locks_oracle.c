@@ -564,3 +564,202 @@ void lo_attend(int batch, int hq, int hkv, int max_pages, const float* q, const 
 
 /* Rounds a real to the nearest fp16 value (exposed for the quantiser pins). */
 double lo_round_f16(double x) { return lo_f16_round(x); }
+
+/* -------------------------------------------------------------- ablations */
+
+/*
+ * Exact page score, the selector that reads every key ([p4] section 1, the
+ * "exact selection" that reads all keys; section 3, the read-all-keys
+ * selector LOCKS is measured against):
+ *   s = log sum_i exp(q . k_i / sqrt(d)) over the 16 keys of the page.
+ * k is one unit's [16][128] bf16 keys.
+ */
+double lo_exact_score_unit(const double* q, const uint16_t* k) {
+    double t[LO_PAGE], mx = -INFINITY;
+    for (int i = 0; i < LO_PAGE; ++i) {
+        double s = 0.0;
+        for (int c = 0; c < LO_D; ++c) s += q[c] * lo_bf16_to_f64(k[i * LO_D + c]);
+        t[i] = s / sqrt((double)LO_D);
+        if (t[i] > mx) mx = t[i];
+    }
+    double z = 0.0;
+    for (int i = 0; i < LO_PAGE; ++i) z += exp(t[i] - mx);
+    return mx + log(z);
+}
+
+/* The physical unit of (b, kv head, logical page j); NULL when j is past the sequence. */
+static const uint16_t* lo_unit_keys(const uint16_t* k_cache, const int32_t* table, const int32_t* seq_pages,
+                                    int hkv, int max_pages, int b, int kvh, int j) {
+    if (j >= seq_pages[b]) return NULL;
+    int64_t phys = table[(int64_t)b * max_pages + j];
+    return k_cache + (phys * hkv + kvh) * (int64_t)(LO_PAGE * LO_D);
+}
+
+/* Exact scores of every (b, h, j < seq_pages[b]); out is [B][Hq][max_pages]. */
+void lo_exact_scores(int batch, int hq, int hkv, int max_pages, const float* q, const uint16_t* k_cache,
+                     const int32_t* table, const int32_t* seq_pages, double* out) {
+    int g = hq / hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 64)
+    for (int b = 0; b < batch; ++b)
+        for (int j = 0; j < max_pages; ++j)
+            for (int kvh = 0; kvh < hkv; ++kvh) {
+                const uint16_t* k = lo_unit_keys(k_cache, table, seq_pages, hkv, max_pages, b, kvh, j);
+                if (!k) continue;
+                for (int hh = 0; hh < g; ++hh) {
+                    int h = kvh * g + hh;
+                    double qq[LO_D];
+                    for (int c = 0; c < LO_D; ++c) qq[c] = q[((int64_t)b * hq + h) * LO_D + c];
+                    out[((int64_t)b * hq + h) * max_pages + j] = lo_exact_score_unit(qq, k);
+                }
+            }
+}
+
+/*
+ * Replaces x[0..n) by its dequantised absmax codes of `bits` bits
+ * (symmetric: qmax = 2^(bits-1) - 1, so int8 -> 127, int4 -> 7, int2 -> 1);
+ * bits = 0 leaves x unquantised. The quantiser is the one of the shipped
+ * summary ([p1] "How LOCKS works": int8 centroid, int4 basis, int8
+ * coefficients), with the width as the ablated parameter ([p1] "Caveats").
+ */
+void lo_quant_dequant(double* x, int n, int bits) {
+    if (bits == 0) return;
+    int codes[LO_D * LO_PAGE];
+    int qmax = (1 << (bits - 1)) - 1;
+    double s = lo_f16_to_f64(lo_quantise(x, n, qmax, codes));
+    for (int i = 0; i < n; ++i) x[i] = (s > 0.0 && !isinf(s)) ? codes[i] * s : 0.0;
+}
+
+/*
+ * Ablation variant of the summary score: the page-local summary of rank
+ * `rank` (1..15; 15 spans all 16 centred keys) built as lo_build_unit_f64
+ * does, mu / V / C each quantised to bits_mu / bits_v / bits_c (8, 4, 2, or
+ * 0 for unquantised, the setting Theorem 1 covers), dequantised and scored
+ * with the summary score formula. Rank 8 with bits (8, 4, 8) is the shipped
+ * summary. out is [B][Hq][max_pages].
+ */
+void lo_variant_scores(int batch, int hq, int hkv, int max_pages, const float* q, const uint16_t* k_cache,
+                       const int32_t* table, const int32_t* seq_pages, int rank, int bits_mu, int bits_v,
+                       int bits_c, double* out) {
+    int g = hq / hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+    for (int b = 0; b < batch; ++b)
+        for (int j = 0; j < max_pages; ++j)
+            for (int kvh = 0; kvh < hkv; ++kvh) {
+                const uint16_t* k = lo_unit_keys(k_cache, table, seq_pages, hkv, max_pages, b, kvh, j);
+                if (!k) continue;
+                double mu[LO_D], basis[LO_D * LO_PAGE], coef[LO_PAGE * LO_PAGE];
+                lo_build_unit_f64(k, rank, mu, basis, coef, NULL);
+                lo_quant_dequant(mu, LO_D, bits_mu);
+                lo_quant_dequant(basis, LO_D * rank, bits_v);
+                lo_quant_dequant(coef, LO_PAGE * rank, bits_c);
+                for (int hh = 0; hh < g; ++hh) {
+                    int h = kvh * g + hh;
+                    double qq[LO_D];
+                    for (int c = 0; c < LO_D; ++c) qq[c] = q[((int64_t)b * hq + h) * LO_D + c];
+                    out[((int64_t)b * hq + h) * max_pages + j] = lo_score_unit(qq, mu, basis, coef, rank);
+                }
+            }
+}
+
+/*
+ * Shared basis of the kind shared-projection selectors use ([p1] "Why
+ * shared-basis sparse attention is structurally broken": one low-rank basis
+ * built from the full sequence): per (request b, kv head), the `rank`
+ * eigenvectors of largest eigenvalue of M = sum_t k_t k_t^T over every token
+ * of the sequence's seq_pages[b] pages (the top right singular vectors of the
+ * sequence's key matrix), by the cyclic Jacobi method, descending (equal
+ * eigenvalues keep the lower index first). A direction with
+ * lambda <= 1e-12 lambda_1 is returned as zeros. Sign: the largest-magnitude
+ * entry (first on ties) is positive. basis is [B][Hkv][rank][128]; eigvals,
+ * if not NULL, gets all 128 eigenvalues of each M ([B][Hkv][128], descending).
+ */
+void lo_shared_basis(int batch, int hkv, int max_pages, const uint16_t* k_cache, const int32_t* table,
+                     const int32_t* seq_pages, int rank, double* basis, double* eigvals) {
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < batch; ++b)
+        for (int kvh = 0; kvh < hkv; ++kvh) {
+            double* m = (double*)calloc(LO_D * LO_D, sizeof(double));
+            double* u = (double*)malloc(LO_D * LO_D * sizeof(double));
+            double kt[LO_D];
+            for (int j = 0; j < seq_pages[b]; ++j) {
+                const uint16_t* k = lo_unit_keys(k_cache, table, seq_pages, hkv, max_pages, b, kvh, j);
+                for (int i = 0; i < LO_PAGE; ++i) {
+                    for (int c = 0; c < LO_D; ++c) kt[c] = lo_bf16_to_f64(k[i * LO_D + c]);
+                    for (int r = 0; r < LO_D; ++r)
+                        for (int c = 0; c < LO_D; ++c) m[r * LO_D + c] += kt[r] * kt[c];
+                }
+            }
+            lo_jacobi_eig(LO_D, m, u, 1e-14, 100);
+            int order[LO_D];
+            for (int i = 0; i < LO_D; ++i) order[i] = i;
+            for (int i = 1; i < LO_D; ++i) {           /* stable insertion sort, descending */
+                int x = order[i], p = i - 1;
+                while (p >= 0 && m[order[p] * LO_D + order[p]] < m[x * LO_D + x]) {
+                    order[p + 1] = order[p];
+                    --p;
+                }
+                order[p + 1] = x;
+            }
+            double* out = basis + ((int64_t)b * hkv + kvh) * rank * LO_D;
+            if (eigvals)
+                for (int i = 0; i < LO_D; ++i)
+                    eigvals[((int64_t)b * hkv + kvh) * LO_D + i] = m[order[i] * LO_D + order[i]];
+            double lam1 = m[order[0] * LO_D + order[0]];
+            for (int r = 0; r < rank; ++r) {
+                int col = order[r];
+                double lam = m[col * LO_D + col];
+                int best = 0;
+                for (int c = 1; c < LO_D; ++c)
+                    if (fabs(u[c * LO_D + col]) > fabs(u[best * LO_D + col])) best = c;
+                double sgn = u[best * LO_D + col] < 0.0 ? -1.0 : 1.0;
+                int keep = lam1 > 0.0 && lam > 1e-12 * lam1;
+                for (int c = 0; c < LO_D; ++c) out[r * LO_D + c] = keep ? sgn * u[c * LO_D + col] : 0.0;
+            }
+            free(m);
+            free(u);
+        }
+}
+
+/*
+ * Shared-basis page score: the keys seen through the fixed projection
+ * P = W W^T of the basis W ([rank][128] rows per (b, kv head)),
+ *   s = log sum_i exp(q . (P k_i) / sqrt(d)),
+ * so a page whose keys lie in the null space of W^T scores log 16 whatever
+ * the query ([p1] "Why shared-basis sparse attention is structurally broken";
+ * Proposition 1 of [p4] section 3). out is [B][Hq][max_pages].
+ */
+void lo_shared_scores(int batch, int hq, int hkv, int max_pages, const float* q, const uint16_t* k_cache,
+                      const int32_t* table, const int32_t* seq_pages, const double* basis, int rank,
+                      double* out) {
+    int g = hq / hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 64)
+    for (int b = 0; b < batch; ++b)
+        for (int j = 0; j < max_pages; ++j)
+            for (int kvh = 0; kvh < hkv; ++kvh) {
+                const uint16_t* k = lo_unit_keys(k_cache, table, seq_pages, hkv, max_pages, b, kvh, j);
+                if (!k) continue;
+                const double* w = basis + ((int64_t)b * hkv + kvh) * rank * LO_D;
+                double pk[LO_PAGE][LO_D];
+                for (int i = 0; i < LO_PAGE; ++i) {
+                    for (int c = 0; c < LO_D; ++c) pk[i][c] = 0.0;
+                    for (int r = 0; r < rank; ++r) {
+                        double a = 0.0;
+                        for (int c = 0; c < LO_D; ++c) a += w[r * LO_D + c] * lo_bf16_to_f64(k[i * LO_D + c]);
+                        for (int c = 0; c < LO_D; ++c) pk[i][c] += a * w[r * LO_D + c];
+                    }
+                }
+                for (int hh = 0; hh < g; ++hh) {
+                    int h = kvh * g + hh;
+                    double t[LO_PAGE], mx = -INFINITY;
+                    for (int i = 0; i < LO_PAGE; ++i) {
+                        double s = 0.0;
+                        for (int c = 0; c < LO_D; ++c) s += q[((int64_t)b * hq + h) * LO_D + c] * pk[i][c];
+                        t[i] = s / sqrt((double)LO_D);
+                        if (t[i] > mx) mx = t[i];
+                    }
+                    double z = 0.0;
+                    for (int i = 0; i < LO_PAGE; ++i) z += exp(t[i] - mx);
+                    out[((int64_t)b * hq + h) * max_pages + j] = mx + log(z);
+                }
+            }
+}
