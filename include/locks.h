@@ -6,11 +6,15 @@
  * the page's keys, and at each decode step reads only those summaries to
  * choose the pages that receive full attention. Source pages:
  *   [post]    "LOCKS: per-page SVD cuts KV cache reads 10x at 1M context"
- *             (wps.hkprog.org), sections "How LOCKS works" and "Code".
+ *             (wps.hkprog.org), sections "How LOCKS works" and "Code"; for
+ *             the ablations also "Why shared-basis sparse attention is
+ *             structurally broken" and "Caveats".
  *   [summary] gist.science technical summary of arXiv 2607.24555, section 2
  *             "Method" (2.1 page-local spectral decomposition, 2.2
  *             reconstruction and selection, 2.3 group-shared selection,
- *             2.4 implementation).
+ *             2.4 implementation); for the ablations also section 1 (problem
+ *             statement: exact selection reads every key) and section 3
+ *             (contributions: Proposition 1, the read-all-keys selector).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -321,6 +325,88 @@ LOCKS_API int locks_set_wait_limit_ns(uint64_t ns);
  */
 LOCKS_API int locks_selftest_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
                                           void* stream);
+
+/* ------------------------------------------------------------------------
+ * Selector ablations (synthetic-carrier studies; not on the decode path).
+ *
+ * These calls score pages by other selectors than the shipped summary, for
+ * recall and mass-coverage studies; the scores go through locks_select_pages
+ * like the summary scores do. All take the decode step's dims, queries
+ * (fp32 [B][Hq][128]), K cache (bf16 bits [num_phys_pages][Hkv][16][128],
+ * 16-byte aligned), page table and seq_pages, and write fp32 scores
+ * [B][Hq][max_pages_per_seq] for j < seq_pages[b] only (other entries are not
+ * written). An out-of-range page-table entry is read as physical page 0 and
+ * recorded as LOCKS_ERR_BAD_INDEX in the workspace status word when a
+ * workspace is given. Asynchronous on `stream`; the caller owns every buffer.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of workspace locks_shared_basis and locks_shared_scores need
+ * (256-byte aligned): the status word, the fp32 second moments
+ * [B][Hkv][128][128] and the projected queries [B][Hq][128].
+ */
+LOCKS_API int locks_ablation_workspace_size(const locks_dims_t* dims, size_t* bytes);
+
+/*
+ * Exact page scores, the selector that reads every key ([summary] sections
+ * 1 and 3: exact selection reads all keys, the reference LOCKS is measured
+ * against):
+ *   scores[b][h][j] = log sum_i exp(q_h . k_i / sqrt(128)) over the 16 keys of
+ *   physical page page_table[b][j], kv head h / (Hq / Hkv).
+ * workspace may be NULL (then no status is recorded). Reads 4 KB per unit.
+ */
+LOCKS_API int locks_exact_scores(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                 const int32_t* page_table, const int32_t* seq_pages, float* scores,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Scores of page-local summaries of another rank or code width, built from the
+ * keys and scored in one pass ([post] "Caveats": int4 loses a few recall
+ * points, int2 collapses; [post] "How LOCKS works" for the summary and its
+ * score; Theorem 1 covers the unquantised rank-r summary). Per unit: mu, the
+ * top-`rank` eigenpairs of the centred keys' 16 x 16 Gram matrix (cyclic
+ * Jacobi), V[:, r] = D^T u_r / sqrt(lambda_r), C[:, r] = sqrt(lambda_r) u_r
+ * (zero where lambda_r <= 1e-12 lambda_1); mu, V and C are each replaced by
+ * their symmetric absmax codes of bits_mu / bits_v / bits_c bits (scale =
+ * fp16(absmax / (2^(bits-1) - 1)), round half to even), or kept when the
+ * width is 0; then the summary score of locks_score_pages. rank 8 with widths
+ * (8, 4, 8) is the shipped summary. rank must be 1..15 (15 spans the 16
+ * centred keys), each width 0 or 2..8, else LOCKS_ERR_INVALID_ARG.
+ */
+LOCKS_API int locks_variant_scores(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                   const int32_t* page_table, const int32_t* seq_pages, int32_t rank,
+                                   int32_t bits_mu, int32_t bits_v, int32_t bits_c, float* scores,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The shared basis a shared-projection selector builds from the full sequence
+ * ([post] "Why shared-basis sparse attention is structurally broken"): per
+ * (b, kv head), the `rank` (0..128) eigenvectors of largest eigenvalue of the
+ * uncentred second moment M = sum_t k_t k_t^T over every token of the
+ * sequence's seq_pages[b] pages (fp32, parallel cyclic Jacobi), written as
+ * rows basis[b][kvh][r][128] (rank-major), each with its largest-magnitude
+ * entry positive, zero where lambda_r <= 1e-12 lambda_1. eigvals (nullable)
+ * receives all 128 eigenvalues of each M in descending order
+ * ([B][Hkv][128]). workspace must hold locks_ablation_workspace_size bytes.
+ */
+LOCKS_API int locks_shared_basis(const locks_dims_t* dims, const uint16_t* k_cache, const int32_t* page_table,
+                                 const int32_t* seq_pages, int32_t rank, float* basis, float* eigvals,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Shared-basis page scores ([post] "Why shared-basis sparse attention is
+ * structurally broken"; Proposition 1, [summary] section 3): the
+ * keys seen through the fixed projection P = W W^T of the basis W
+ * (basis[b][kvh][rank][128], orthonormal rows, e.g. from locks_shared_basis),
+ *   scores[b][h][j] = log sum_i exp(q_h . (P k_i) / sqrt(128)),
+ * computed as the exact score of the projected query P q_h (P is symmetric).
+ * A page whose keys lie in the null space of W^T scores log 16 for any query.
+ * workspace must hold locks_ablation_workspace_size bytes.
+ */
+LOCKS_API int locks_shared_scores(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                                  const int32_t* page_table, const int32_t* seq_pages, const float* basis,
+                                  int32_t rank, float* scores, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

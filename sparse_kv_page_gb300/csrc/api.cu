@@ -426,6 +426,139 @@ int locks_selftest_bounded_wait(void* workspace, size_t workspace_bytes, uint64_
 
 }  // extern "C"
 
+// ------------------------------------------------------------- ablations
+
+namespace {
+
+struct AbLayout {
+    size_t moment, q_proj, total;
+};
+AbLayout ab_layout(const locks_dims_t* d) {
+    AbLayout w;
+    const size_t B = static_cast<size_t>(d->batch);
+    w.moment = kAlign;
+    w.q_proj = w.moment + align_up(B * d->num_kv_heads * 128 * 128 * sizeof(float));
+    w.total = w.q_proj + align_up(B * d->num_q_heads * 128 * sizeof(float));
+    return w;
+}
+
+locks::AblationArgs ab_args(const locks_dims_t* d, const float* q, const uint16_t* k_cache,
+                            const int32_t* page_table, const int32_t* seq_pages, void* ws) {
+    locks::AblationArgs a = {};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.page_table = page_table;
+    a.seq_pages = seq_pages;
+    a.batch = d->batch;
+    a.hq = d->num_q_heads;
+    a.hkv = d->num_kv_heads;
+    a.max_pages = d->max_pages_per_seq;
+    a.num_phys = d->num_phys_pages;
+    a.st = status_of(ws);
+    return a;
+}
+
+// Common checks of the ablation calls; LOCKS_OK means "launch".
+int ab_check(const locks_dims_t* d, const uint16_t* k_cache, const int32_t* page_table,
+             const int32_t* seq_pages) {
+    int v = validate_dims(d);
+    if (v != LOCKS_OK) return v;
+    if (d->batch > 0 && (!k_cache || !page_table || !seq_pages)) return LOCKS_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16)) return LOCKS_ERR_INVALID_ARG;
+    if (static_cast<long>(d->max_pages_per_seq + 127) / 64 > 65535) return LOCKS_ERR_UNSUPPORTED;
+    if (current_device() < 0) return LOCKS_ERR_CUDA;
+    return LOCKS_OK;
+}
+
+bool valid_bits(int32_t b) { return b == 0 || (b >= 2 && b <= 8); }
+
+}  // namespace
+
+extern "C" {
+
+int locks_ablation_workspace_size(const locks_dims_t* dims, size_t* bytes) {
+    if (!bytes) return LOCKS_ERR_INVALID_ARG;
+    const int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    *bytes = ab_layout(dims).total;
+    return LOCKS_OK;
+}
+
+int locks_exact_scores(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                       const int32_t* page_table, const int32_t* seq_pages, float* scores, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    int v = ab_check(dims, k_cache, page_table, seq_pages);
+    if (v != LOCKS_OK) return v;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!q || !scores) return LOCKS_ERR_INVALID_ARG;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    locks::AblationArgs a = ab_args(dims, q, k_cache, page_table, seq_pages, workspace);
+    a.scores = scores;
+    return cuda_status(locks::launch_exact_scores(a, static_cast<cudaStream_t>(stream)));
+}
+
+int locks_variant_scores(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                         const int32_t* page_table, const int32_t* seq_pages, int32_t rank, int32_t bits_mu,
+                         int32_t bits_v, int32_t bits_c, float* scores, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    int v = ab_check(dims, k_cache, page_table, seq_pages);
+    if (v != LOCKS_OK) return v;
+    if (rank < 1 || rank > 15 || !valid_bits(bits_mu) || !valid_bits(bits_v) || !valid_bits(bits_c))
+        return LOCKS_ERR_INVALID_ARG;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!q || !scores) return LOCKS_ERR_INVALID_ARG;
+    if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
+    locks::AblationArgs a = ab_args(dims, q, k_cache, page_table, seq_pages, workspace);
+    a.scores = scores;
+    a.rank = rank;
+    a.bits_mu = bits_mu;
+    a.bits_v = bits_v;
+    a.bits_c = bits_c;
+    return cuda_status(locks::launch_variant_scores(a, static_cast<cudaStream_t>(stream)));
+}
+
+int locks_shared_basis(const locks_dims_t* dims, const uint16_t* k_cache, const int32_t* page_table,
+                       const int32_t* seq_pages, int32_t rank, float* basis, float* eigvals, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    int v = ab_check(dims, k_cache, page_table, seq_pages);
+    if (v != LOCKS_OK) return v;
+    if (rank < 0 || rank > 128) return LOCKS_ERR_INVALID_ARG;
+    const AbLayout L = ab_layout(dims);
+    if ((v = check_ws(workspace, workspace_bytes, L.total)) != LOCKS_OK) return v;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (rank > 0 && !basis) return LOCKS_ERR_INVALID_ARG;
+    locks::AblationArgs a = ab_args(dims, nullptr, k_cache, page_table, seq_pages, workspace);
+    a.rank = rank;
+    a.moment = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.moment);
+    a.basis = basis;
+    a.eigvals = eigvals;
+    return cuda_status(locks::launch_shared_basis(a, static_cast<cudaStream_t>(stream)));
+}
+
+int locks_shared_scores(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
+                        const int32_t* page_table, const int32_t* seq_pages, const float* basis, int32_t rank,
+                        float* scores, void* workspace, size_t workspace_bytes, void* stream) {
+    int v = ab_check(dims, k_cache, page_table, seq_pages);
+    if (v != LOCKS_OK) return v;
+    if (rank < 0 || rank > 128) return LOCKS_ERR_INVALID_ARG;
+    const AbLayout L = ab_layout(dims);
+    if ((v = check_ws(workspace, workspace_bytes, L.total)) != LOCKS_OK) return v;
+    if (dims->batch == 0) return LOCKS_OK;
+    if (!q || !scores || (rank > 0 && !basis)) return LOCKS_ERR_INVALID_ARG;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* qp = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.q_proj);
+    locks::AblationArgs a = ab_args(dims, q, k_cache, page_table, seq_pages, workspace);
+    a.rank = rank;
+    a.basis = const_cast<float*>(basis);
+    a.q_proj = qp;
+    if ((v = cuda_status(locks::launch_project_queries(a, st))) != LOCKS_OK) return v;
+    a.q = qp;
+    a.scores = scores;
+    return cuda_status(locks::launch_exact_scores(a, st));
+}
+
+}  // extern "C"
+
 namespace locks {
 
 // One thread waits on an mbarrier whose phase nothing completes (expected

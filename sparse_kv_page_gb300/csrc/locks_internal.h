@@ -94,6 +94,28 @@ struct BuildArgs {
 };
 cudaError_t launch_build(const BuildArgs& a, int num_sms, cudaStream_t stream);
 
+// Selector ablations (off the decode path). One argument block for the five kernels;
+// each uses the fields its comment names.
+struct AblationArgs {
+    const float* q;           // [B][Hq][128]: queries (exact, variant, projection) or projected queries
+    const uint16_t* k_cache;  // [num_phys][hkv][16][128] bf16
+    const int32_t* page_table;
+    const int32_t* seq_pages;
+    float* scores;            // [B][Hq][max_pages] (exact, variant)
+    int batch, hq, hkv, max_pages, num_phys;
+    int rank;                 // variant: 1..15; shared basis / projection: 0..128
+    int bits_mu, bits_v, bits_c;   // variant: 0 (unquantised) or 2..8
+    float* moment;            // [B][Hkv][128][128] fp32 second moments (shared basis)
+    float* basis;             // [B][Hkv][rank][128] (written by the shared basis, read by the projection)
+    float* eigvals;           // nullable [B][Hkv][128] (shared basis)
+    float* q_proj;            // [B][Hq][128] (projection output)
+    DeviceStatus st;
+};
+cudaError_t launch_exact_scores(const AblationArgs& a, cudaStream_t stream);
+cudaError_t launch_variant_scores(const AblationArgs& a, cudaStream_t stream);
+cudaError_t launch_shared_basis(const AblationArgs& a, cudaStream_t stream);
+cudaError_t launch_project_queries(const AblationArgs& a, cudaStream_t stream);
+
 // Bounded-wait self test: one CTA waits on an mbarrier phase that never
 // completes and must give up after the limit, recording LOCKS_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(DeviceStatus st, cudaStream_t stream);

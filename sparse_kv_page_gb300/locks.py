@@ -89,6 +89,11 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             "locks_clear_device_status": ([P, P], ctypes.c_int),
             "locks_set_wait_limit_ns": ([U64], ctypes.c_int),
             "locks_selftest_bounded_wait": ([P, S, U64, P], ctypes.c_int),
+            "locks_ablation_workspace_size": ([D, ctypes.POINTER(S)], ctypes.c_int),
+            "locks_exact_scores": ([D, P, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_variant_scores": ([D, P, P, P, P, I32, I32, I32, I32, P, P, S, P], ctypes.c_int),
+            "locks_shared_basis": ([D, P, P, P, I32, P, P, P, S, P], ctypes.c_int),
+            "locks_shared_scores": ([D, P, P, P, P, P, I32, P, P, S, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -276,3 +281,48 @@ def locks_selftest_bounded_wait(workspace, limit_ns: int, stream=None) -> None:
     ws, nws = _ws(workspace)
     _check("locks_selftest_bounded_wait",
            load_library().locks_selftest_bounded_wait(ws, nws, int(limit_ns), _stream(stream)))
+
+
+# --------------------------------------------------------------- ablations
+
+def locks_ablation_workspace_size(dims: locks_dims_t) -> int:
+    out = ctypes.c_size_t(0)
+    _check("locks_ablation_workspace_size", load_library().locks_ablation_workspace_size(ctypes.byref(dims),
+                                                                                       ctypes.byref(out)))
+    return out.value
+
+
+def alloc_ablation_workspace(dims: locks_dims_t, device="cuda") -> torch.Tensor:
+    """A zeroed workspace of locks_ablation_workspace_size bytes."""
+    return torch.zeros(max(locks_ablation_workspace_size(dims), 256), dtype=torch.uint8, device=device)
+
+
+def locks_exact_scores(dims, q, k_cache, page_table, seq_pages, scores, workspace=None, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_exact_scores", load_library().locks_exact_scores(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(page_table), _ptr(seq_pages), _ptr(scores), ws, nws,
+        _stream(stream)))
+
+
+def locks_variant_scores(dims, q, k_cache, page_table, seq_pages, rank, bits_mu, bits_v, bits_c, scores,
+                         workspace=None, stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_variant_scores", load_library().locks_variant_scores(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(page_table), _ptr(seq_pages), int(rank), int(bits_mu),
+        int(bits_v), int(bits_c), _ptr(scores), ws, nws, _stream(stream)))
+
+
+def locks_shared_basis(dims, k_cache, page_table, seq_pages, rank, basis, workspace, eigvals=None,
+                       stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_shared_basis", load_library().locks_shared_basis(
+        ctypes.byref(dims), _ptr(k_cache), _ptr(page_table), _ptr(seq_pages), int(rank), _ptr(basis),
+        _ptr(eigvals), ws, nws, _stream(stream)))
+
+
+def locks_shared_scores(dims, q, k_cache, page_table, seq_pages, basis, rank, scores, workspace,
+                        stream=None) -> None:
+    ws, nws = _ws(workspace)
+    _check("locks_shared_scores", load_library().locks_shared_scores(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(page_table), _ptr(seq_pages), _ptr(basis), int(rank),
+        _ptr(scores), ws, nws, _stream(stream)))
