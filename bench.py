@@ -539,6 +539,13 @@ def run_locks(args, rank, world, local):
                          "same attention kernel), one CUDA graph, L2 flushed before each"}
         assert L.locks_get_device_status(ws) == 0, "device status after the dense comparator"
 
+    # selector ablations (outside the timed region): recall, attention mass and carrier retention of
+    # the shipped summary, other ranks / code widths and shared bases against the exact selection
+    ablation = None
+    if rank == 0 and not args.no_ablation:
+        from sparse_kv_page_gb300 import ablation as AB
+        ablation = AB.run(dims, q, kc, table, seq, summ, budget, inp.carriers, dev)
+
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -568,6 +575,7 @@ def run_locks(args, rank, world, local):
         "dense_comparator": dense,
         "model_graph": model_graph,
         "page_refresh": refresh,
+        "ablation": ablation,
         "roofline": {"kernel": "score_pages (locks_score_pages)", "bound": "hbm", "achieved": score_gbs,
                      "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
                      "frac": score_gbs / hbm,
@@ -599,6 +607,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
     ap.add_argument("--no-model-graph", action="store_true", help="skip the 32-layer decode graph")
+    ap.add_argument("--no-ablation", action="store_true", help="skip the selector ablations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

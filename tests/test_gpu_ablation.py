@@ -203,3 +203,30 @@ def test_ablation_argument_errors():
         L.locks_shared_basis(dims, kd, td, sd, 8, basis, small)
     with pytest.raises(L.LocksError):
         L.locks_shared_basis(dims, kd, td, sd, 129, basis, L.alloc_ablation_workspace(dims, DEV))
+
+
+def test_ablation_harness_properties():
+    """On a shortened benchmark workload: the exact selection holds the most mass any k pages
+    can hold, rank 15 unquantised reproduces it, and the variant kernel at the shipped
+    widths agrees with the shipped summary path."""
+    from sparse_kv_page_gb300 import ablation as AB
+
+    w = synth.WORKLOADS["ctx1m"].scaled(pages=1024)
+    inp = synth.make_decode_inputs(w, with_values=False)
+    dims = L.make_dims(w.batch, w.num_q_heads, w.num_kv_heads, w.pages, w.num_phys_pages)
+    kc = t(inp.k_cache)
+    summ = L.Summaries.empty(w.num_phys_pages, w.num_kv_heads, DEV)
+    L.locks_build_summaries(dims, kc, torch.arange(w.num_phys_pages, dtype=torch.int32, device=DEV),
+                            w.num_phys_pages, summ)
+    rec = AB.run(dims, t(inp.q), kc, t(inp.page_table), t(inp.seq_pages), summ, 512, inp.carriers, DEV)
+    rows = {r["selector"]: r for r in rec["rows"]}
+    exact = rows["exact (reads every key)"]
+    assert exact["recall"] == 1.0 and exact["carriers_kept"] >= 0.9
+    for r in rec["rows"]:
+        assert 0.0 <= r["recall"] <= 1.0 and 0.0 <= r["carriers_kept"] <= 1.0
+        assert r["mass"] <= exact["mass"] + 1e-4, r
+    assert rows["r15 unquantised"]["recall"] >= 0.99
+    shipped = rows["r8 int8/int4/int8 (shipped summary, locks_score_pages)"]
+    variant = rows["r8 int8/int4/int8 (variant kernel)"]
+    assert abs(shipped["recall"] - variant["recall"]) <= 0.02
+    assert shipped["recall"] >= 0.8
