@@ -39,6 +39,9 @@ constexpr int kEigN = 128;
 constexpr int kEigStride = 129;
 constexpr int kSmallSweeps = 12;     // 16 x 16 Jacobi
 constexpr int kLargeSweeps = 30;     // 128 x 128 Jacobi
+// A sweep that shrinks the off-diagonal energy by less than 10% has reached the
+// fp32 rounding floor (Jacobi converges quadratically until then): stop there.
+constexpr float kStallRatio = 0.9f;
 
 __device__ __forceinline__ int seq_len(const AblationArgs& a, int b) {
     const int p = a.seq_pages[b];
@@ -122,13 +125,20 @@ __global__ void __launch_bounds__(kAbWarps * 32) exact_kernel(AblationArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tok = lane & 15, half = lane >> 4;
     const int j1 = min(P, j0 + kAbPagesPerCta);
-    for (int j = j0 + warp; j < j1; j += kAbWarps) {
+    auto load_unit = [&](int j, uint4 (&dst)[8]) {
         const int64_t phys = phys_page(a, b, j);
         const uint4* src = reinterpret_cast<const uint4*>(
             a.k_cache + ((phys * a.hkv + kvh) * kPage + tok) * kD + half * 64);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) dst[v] = src[v];
+    };
+    uint4 nxt[8];   // the warp's next unit, loaded while the current one is scored
+    if (j0 + warp < j1) load_unit(j0 + warp, nxt);
+    for (int j = j0 + warp; j < j1; j += kAbWarps) {
         float k[64];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) bf16x8_to_f32(src[v], k + 8 * v);
+        for (int v = 0; v < 8; ++v) bf16x8_to_f32(nxt[v], k + 8 * v);
+        if (j + kAbWarps < j1) load_unit(j + kAbWarps, nxt);
         for (int hh = 0; hh < g; ++hh) {
             const float4* qv = reinterpret_cast<const float4*>(qs + hh * kD + half * 64);
             float d0 = 0.f, d1 = 0.f;
@@ -214,7 +224,7 @@ __device__ void quant_dequant(float* x, int rows, int cols, int stride, int bits
 
 // Grid (B * Hkv, runs of 64 pages); dynamic shared memory = the group's
 // queries, then one VariantWarp per warp.
-__global__ void __launch_bounds__(kAbWarps * 32) variant_kernel(AblationArgs a) {
+__global__ void __launch_bounds__(kAbWarps * 32, 2) variant_kernel(AblationArgs a) {
     extern __shared__ __align__(16) unsigned char ab_smem[];
     const int g = a.hq / a.hkv;
     float* qs = reinterpret_cast<float*>(ab_smem);
@@ -279,6 +289,7 @@ __global__ void __launch_bounds__(kAbWarps * 32) variant_kernel(AblationArgs a) 
             }
         }
         __syncwarp();
+        float prev_off = INFINITY;
         for (int sweep = 0; sweep < kSmallSweeps; ++sweep) {   // cyclic Jacobi, round-robin order
             float off = 0.f, tot = 0.f;
             for (int e = lane; e < kPage * kPage; e += 32) {
@@ -288,7 +299,9 @@ __global__ void __launch_bounds__(kAbWarps * 32) variant_kernel(AblationArgs a) 
             }
             off = __shfl_sync(0xffffffffu, warp_sum(off), 0);
             tot = __shfl_sync(0xffffffffu, warp_sum(tot), 0);
-            if (!(off > 1e-14f * tot)) break;   // converged (also for an all-zero or NaN page)
+            // converged (also for an all-zero or NaN page), or at the fp32 rounding floor
+            if (!(off > 1e-14f * tot) || !(off < kStallRatio * prev_off)) break;
+            prev_off = off;
             for (int r = 0; r < 15; ++r) {
                 if (lane < 8) {   // round r pairs (r, 15) and ((r + k) mod 15, (r - k) mod 15), k = 1..7
                     const int p = lane == 0 ? r : (r + lane) % 15;
@@ -442,7 +455,7 @@ __global__ void __launch_bounds__(256) moment_kernel(AblationArgs a) {
 }
 
 constexpr int eig_smem_bytes() {
-    return 2 * kEigN * kEigStride * 4 + 64 * 8 + 64 * 8 + kEigN * 4 + 36 * 4;
+    return 2 * kEigN * kEigStride * 4 + 64 * 8 + 64 * 8 + kEigN * 4 + 36 * 4;   // red: 34 floats used
 }
 
 // One CTA per (b, kv head): cyclic Jacobi on the symmetrised moment in
@@ -458,7 +471,7 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(AblationArgs a) {
     float2* cs = reinterpret_cast<float2*>(V + kEigN * kEigStride);
     int2* pq = reinterpret_cast<int2*>(cs + 64);
     int* ord = reinterpret_cast<int*>(pq + 64);
-    float* red = reinterpret_cast<float*>(ord + kEigN);   // [16] off, [16] total, [1] flag
+    float* red = reinterpret_cast<float*>(ord + kEigN);   // [16] off, [16] total, flag, off of the sweep
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t bk = blockIdx.x;
     const float* M = a.moment + bk * kD * kD;
@@ -468,6 +481,7 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(AblationArgs a) {
         V[i * kEigStride + j] = (i == j) ? 1.f : 0.f;
     }
     __syncthreads();
+    float prev_off = INFINITY;
     for (int sweep = 0; sweep < kLargeSweeps; ++sweep) {
         float off = 0.f, tot = 0.f;
         for (int e = t; e < kD * kD; e += kEigThreads) {
@@ -483,18 +497,20 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(AblationArgs a) {
             red[16 + warp] = tot;
         }
         __syncthreads();
-        if (t == 0) {
+        if (t == 0) {   // go on unless converged or at the fp32 rounding floor
             float o = 0.f, s = 0.f;
             for (int x = 0; x < kEigThreads / 32; ++x) {
                 o += red[x];
                 s += red[16 + x];
             }
-            red[32] = (o > 1e-12f * s) ? 1.f : 0.f;
+            red[32] = (o > 1e-12f * s && o < kStallRatio * prev_off) ? 1.f : 0.f;
+            red[33] = o;
         }
         __syncthreads();
         const bool go = red[32] != 0.f;
         __syncthreads();
         if (!go) break;
+        prev_off = red[33];
         for (int r = 0; r < kEigN - 1; ++r) {
             if (t < 64) {
                 const int p = t == 0 ? r : (r + t) % 127;
