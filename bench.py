@@ -359,16 +359,23 @@ def run_locks(args, rank, world, local):
         L.locks_select_attend(dims, q, kc, vc, table, scores, seq, budget, sel, nsel, out, lse, ws,
                               lse_partials=partials)
 
-    # eager warm-up (first-call set-up), then one CUDA graph per kernel of the step
+    # eager warm-up (first-call set-up), then CUDA graphs: the whole step (the two kernels
+    # locks_decode_step launches, the selection programmatically dependent on the scorer) for
+    # the timed steps, and one graph per kernel for the per-kernel breakdown
     score()
     select_attend()
     torch.cuda.synchronize()
-    g_score, g_sa = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_score, g_sa, g_step = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_score):
         score()
     with torch.cuda.graph(g_sa):
         select_attend()
+    with torch.cuda.graph(g_step):
+        score()
+        select_attend()
     for _ in range(args.warmup):
+        flush.zero_()
+        g_step.replay()
         flush.zero_()
         g_score.replay()
         g_sa.replay()
@@ -376,7 +383,8 @@ def run_locks(args, rank, world, local):
     assert L.locks_get_device_status(ws) == 0, "device status after warm-up"
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -390,18 +398,26 @@ def run_locks(args, rank, world, local):
     for i in range(K):
         flush.zero_()
         evs[i][0].record(stream)
-        g_score.replay()
+        g_step.replay()
         evs[i][1].record(stream)
-        g_sa.replay()
-        evs[i][2].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    # per-kernel breakdown: the same K steps with an event between the two kernels
+    for i in range(K):
+        flush.zero_()
+        evk[i][0].record(stream)
+        g_score.replay()
+        evk[i][1].record(stream)
+        g_sa.replay()
+        evk[i][2].record(stream)
+    torch.cuda.synchronize()
     barrier(world)
     sampler.stop()
     status = L.locks_get_device_status(ws)
-    step_ms = [a.elapsed_time(c) for a, _, c in evs]
-    score_ms = [a.elapsed_time(b) for a, b, _ in evs]
-    sa_ms = [b.elapsed_time(c) for _, b, c in evs]
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    score_ms = [a.elapsed_time(b) for a, b, _ in evk]
+    sa_ms = [b.elapsed_time(c) for _, b, c in evk]
+    split_ms = [a.elapsed_time(c) for a, _, c in evk]
     mean_step_us = reduce_max(statistics.mean(step_ms) * 1000.0, world, dev)
     mean_score_us = reduce_max(statistics.mean(score_ms) * 1000.0, world, dev)
     mean_sa_us = reduce_max(statistics.mean(sa_ms) * 1000.0, world, dev)
@@ -570,7 +586,8 @@ def run_locks(args, rank, world, local):
         "frac_of_measured_hbm": step_gbs / hbm, "frac_of_8TBps": step_gbs / NOMINAL_HBM_GBS,
         "aggregate_effective_GBps": step_gbs * world,
         "kernels_us": {"score_pages": mean_score_us, "select_attend": mean_sa_us,
-                       "step_p50": statistics.median(step_ms) * 1000.0},
+                       "step_p50": statistics.median(step_ms) * 1000.0,
+                       "step_two_graphs": statistics.mean(split_ms) * 1000.0},
         "bytes_vs_dense": (w.batch * w.pages * w.num_kv_heads * PAGE_KV_BYTES) / step_bytes,
         "dense_comparator": dense,
         "model_graph": model_graph,
@@ -586,7 +603,9 @@ def run_locks(args, rank, world, local):
         "e2e": {"value": e2e_value, "unit": "us", "h2d_bytes_per_step": int(q_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host.numel() * 2),
                 "path": "pinned q -> locks_decode_step -> output to pinned host, synchronised, wall clock"},
-        "launch": "one CUDA graph per kernel (score_pages, select_attend), replayed each step",
+        "launch": "timed steps: one CUDA graph per step (score_pages, then select_attend launched "
+                  "programmatically dependent on it), L2 flushed before each; kernels_us: a second pass of "
+                  "K steps with one graph per kernel and an event between them",
         "clocks": clocks, "gpu_launches": 2 * K, "device_status": status,
         "timed_wall_s": wall,
         "build": {"units": units, "ms": build_ms, "pages_per_s": w.batch * w.pages / (build_ms * 1e-3),

@@ -277,6 +277,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; grid_dependency_wait() returns once that kernel has completed and
+// its memory is visible, so it must precede the first global access. A kernel
+// that calls allow_dependent_launch() lets its dependents be scheduled once
+// every one of its CTAs has made the call (or exited).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -65,6 +65,10 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
     uint64_t* empty = full + kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The grid is persistent (at most one CTA per SM, every CTA resident from the
+    // start), so a dependent kernel (the selection) only takes SMs this kernel has
+    // left; it may be scheduled as soon as they free up.
+    allow_dependent_launch();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 33);              // 1 expect_tx arrive + 32 LDGSTS arrives

@@ -792,6 +792,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     const int b = seg / a.hkv, kvh = seg % a.hkv;
     if (threadIdx.x < kWarps) mbar_init(&sh.bar[threadIdx.x], 1);
     fence_barrier_init();
+    // launched with programmatic stream serialization: the set-up above overlaps
+    // the end of the previous kernel (the scorer); every global access follows
+    grid_dependency_wait();
     __syncthreads();
 
     if constexpr (MODE == SAMode::kSelect) {
@@ -869,13 +872,15 @@ cudaError_t launch_t(const SelectAttendArgs& args, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, a, chunk);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
