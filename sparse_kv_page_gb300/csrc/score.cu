@@ -65,9 +65,9 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
     uint64_t* empty = full + kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // The grid is persistent (at most one CTA per SM, every CTA resident from the
-    // start), so a dependent kernel (the selection) only takes SMs this kernel has
-    // left; it may be scheduled as soon as they free up.
+    // The grid is persistent (at most one CTA per SM), so a dependent kernel (the
+    // selection) only takes SMs this kernel has left; it may be scheduled as soon
+    // as they free up (the trigger completes once every CTA has started).
     allow_dependent_launch();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -76,6 +76,9 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
         }
         fence_barrier_init();
     }
+    // launched with programmatic stream serialization: the set-up above overlaps
+    // the end of the previous kernel; every global access follows
+    grid_dependency_wait();
     __syncthreads();
 
     const int per = (total_items + gridDim.x - 1) / gridDim.x;
@@ -434,9 +437,17 @@ cudaError_t launch_t(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
     if (total == 0) return cudaSuccess;
     cudaError_t e = ensure_kernel_attrs<score_kernel<HKV, NT, HS>>(kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = min(total, num_sms);
-    score_kernel<HKV, NT, HS><<<grid, Shape<NT>::kThreads, kSmemBytes, stream>>>(a, nchunks, total);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(min(total, num_sms), 1, 1);
+    cfg.blockDim = dim3(Shape<NT>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, score_kernel<HKV, NT, HS>, a, nchunks, total);
 }
 
 template <int HKV>

@@ -790,6 +790,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     const uint32_t rank = cluster_ctarank();
     const int seg = blockIdx.y;
     const int b = seg / a.hkv, kvh = seg % a.hkv;
+    // a dependent kernel (the next layer's scorer) may be scheduled once every CTA
+    // of this grid has started; it waits for this grid's completion itself
+    allow_dependent_launch();
     if (threadIdx.x < kWarps) mbar_init(&sh.bar[threadIdx.x], 1);
     fence_barrier_init();
     // launched with programmatic stream serialization: the set-up above overlaps
