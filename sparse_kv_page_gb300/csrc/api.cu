@@ -2,6 +2,7 @@
 // layout and kernel launches. No allocation, no host synchronisation (except
 // locks_get_device_status), so every compute call can be captured in a CUDA
 // graph.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -39,7 +40,9 @@ int num_sms(int dev) {
 // at once the launch runs in waves, so the choice minimises
 // waves x (pages per CTA + a fixed per-CTA cost in page units). Residency
 // counts come from the occupancy API, cached per (device, mode, group, pages).
-int cluster_size(int dev, const locks_dims_t* d, locks::SAMode mode) {
+// Co-resident 16- and 8-CTA clusters of the select/attend kernel (occupancy API),
+// cached per (device, mode, group bound, pages).
+void active_clusters(int dev, const locks_dims_t* d, locks::SAMode mode, int* a16_out, int* a8_out) {
     struct Entry {
         int dev, mode, gbound, max_pages;
         int active16, active8;
@@ -65,6 +68,13 @@ int cluster_size(int dev, const locks_dims_t* d, locks::SAMode mode) {
             if (n < 128) table[n++] = {dev, static_cast<int>(mode), gbound, d->max_pages_per_seq, a16, a8};
         }
     }
+    *a16_out = a16;
+    *a8_out = a8;
+}
+
+int cluster_size(int dev, const locks_dims_t* d, locks::SAMode mode) {
+    int a16 = 0, a8 = 0;
+    active_clusters(dev, d, mode, &a16, &a8);
     const long segs = static_cast<long>(d->batch) * d->num_kv_heads;
     auto cost = [&](int cl, int active) -> double {
         if (active <= 0) return 1e30;
@@ -103,7 +113,7 @@ int k_cap_of(const locks_dims_t* d, int32_t budget) {
 }
 
 struct WsLayout {
-    size_t status, scores, partials, selected, n_selected, total;
+    size_t status, scores, partials, selected, n_selected, split_cnt, split_part, split_end, total;
 };
 WsLayout ws_layout(const locks_dims_t* d, int32_t budget) {
     WsLayout w;
@@ -114,7 +124,38 @@ WsLayout ws_layout(const locks_dims_t* d, int32_t budget) {
     w.selected = w.partials + align_up(B * d->num_q_heads * static_cast<size_t>((d->max_pages_per_seq + 7) / 8) * 8);
     w.n_selected = w.selected + align_up(B * d->num_kv_heads * static_cast<size_t>(k_cap_of(d, budget)) * 4);
     w.total = w.n_selected + align_up(B * d->num_kv_heads * 4);
+    // split attention (attention-only calls, never alongside the regions above)
+    w.split_cnt = kAlign;
+    w.split_part = w.split_cnt + align_up(B * d->num_q_heads * 4);
+    w.split_end =
+        w.split_part + align_up(B * d->num_q_heads * locks::kMaxSplits * locks::kSplitPartFloats * sizeof(float));
+    if (w.split_end > w.total) w.total = w.split_end;
     return w;
+}
+
+// An attention-only launch over up to k_cap pages per segment: the cluster size and
+// the number of clusters per segment. Long selections are split over more clusters
+// (merged through the workspace) while all of them stay co-resident and each CTA
+// keeps at least kMinSplitPages pages; otherwise one cluster per segment.
+constexpr int kMinSplitPages = 64;
+void attention_plan(int dev, const locks_dims_t* d, int k_cap, bool can_split, int* cl, int* splits) {
+    *cl = cluster_size(dev, d, locks::SAMode::kAttend);
+    *splits = 1;
+    if (!can_split) return;
+    int a16 = 0, a8 = 0;
+    active_clusters(dev, d, locks::SAMode::kAttend, &a16, &a8);
+    const long segs = static_cast<long>(d->batch) * d->num_kv_heads;
+    long best = *cl;
+    for (int c : {16, 8}) {
+        const long act = c == 16 ? a16 : a8;
+        long sp = std::min<long>(locks::kMaxSplits, act / std::max<long>(segs, 1));
+        sp = std::min<long>(sp, k_cap / (static_cast<long>(c) * kMinSplitPages));
+        if (sp >= 2 && c * sp > best) {
+            best = c * sp;
+            *cl = c;
+            *splits = static_cast<int>(sp);
+        }
+    }
 }
 
 int check_ws(void* ws, size_t bytes, size_t need) {
@@ -328,8 +369,20 @@ int locks_sparse_attention(const locks_dims_t* dims, const float* q, const uint1
     a.page_table = page_table;
     a.out = out;
     a.lse = lse;
-    const int cl = cluster_size(dev, dims, locks::SAMode::kAttend);
-    return cuda_status(locks::launch_select_attend(a, locks::SAMode::kAttend, cl, static_cast<cudaStream_t>(stream)));
+    const WsLayout L = ws_layout(dims, k_cap * LOCKS_PAGE_SIZE);
+    const bool can_split = workspace && workspace_bytes >= L.split_end;
+    int cl = 16, splits = 1;
+    attention_plan(dev, dims, k_cap, can_split, &cl, &splits);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (splits > 1) {
+        uint8_t* base = static_cast<uint8_t*>(workspace);
+        a.splits = splits;
+        a.attn_cnt = reinterpret_cast<int32_t*>(base + L.split_cnt);
+        a.attn_part = reinterpret_cast<float*>(base + L.split_part);
+        v = cuda_status(cudaMemsetAsync(a.attn_cnt, 0, static_cast<size_t>(dims->batch) * dims->num_q_heads * 4, st));
+        if (v != LOCKS_OK) return v;
+    }
+    return cuda_status(locks::launch_select_attend(a, locks::SAMode::kAttend, cl, st));
 }
 
 int locks_select_attend(const locks_dims_t* dims, const float* q, const uint16_t* k_cache, const uint16_t* v_cache,

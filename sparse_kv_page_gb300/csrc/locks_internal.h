@@ -67,6 +67,11 @@ struct SelectAttendArgs {
     const int32_t* tail_tokens;   // nullable: tokens of each sequence's unfilled page (fused mode)
     uint16_t* out;
     float* lse;               // nullable
+    // split attention (attention-only launches): `splits` clusters per (sequence, kv
+    // head); per (b, q head) a zeroed arrival count and kMaxSplits (m, l, o[128]) partials
+    int splits;
+    int32_t* attn_cnt;        // nullable: no split
+    float* attn_part;
     int batch, hq, hkv, max_pages, num_phys;
     DeviceStatus st;
     // K and V caches as 2D tensors [num_phys * hkv * 16 rows][128] bf16 for tiled TMA:
@@ -74,6 +79,8 @@ struct SelectAttendArgs {
     CUtensorMap tm_k, tm_v;
 };
 enum class SAMode { kSelect, kAttend, kSelectAttend };
+constexpr int kMaxSplits = 4;
+constexpr int kSplitPartFloats = 2 + 128;   // m, l, o[128] per (b, q head, split)
 cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream);
 // Clusters of `cluster` CTAs (8 or 16) of the select/attend kernel that can be
 // resident at once on the current device (0 if it cannot launch).

@@ -40,6 +40,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBoxBytes = kPage * 64 * 2;             // 2048 B
 constexpr int kPageSlotBytes = 4 * kBoxBytes;         // 8192 B
 constexpr int kPartStride = 2 + kD;                   // m, l, o[128]
+static_assert(kPartStride == kSplitPartFloats, "split partials use the attention partial layout");
 // the ring also holds the warps' attention partials after the page loop
 constexpr int kWarpPartBytes = kWarps * LOCKS_MAX_GROUP * kPartStride * 4;
 constexpr int kRingBytes = ((kWarps * kPageSlotBytes > kWarpPartBytes ? kWarps * kPageSlotBytes : kWarpPartBytes) +
@@ -64,6 +65,7 @@ struct SmallShared {
     uint8_t rank_src[256];
     uint64_t bar[kWarps];
     float cpart[kMaxG * kPartStride];     // this CTA's attention partial per head
+    int split_last;                       // split attention: this cluster merges the splits of a head
 };
 
 // Byte offset of (token row, dim) in a page slot's K (or V) half: box = dim / 64,
@@ -565,9 +567,14 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
         }
     }
     const int n_all = n_sel + (tail + kPage - 1) / kPage;
-    const int per = (n_all + CL - 1) / CL;
-    const int p0 = min(n_all, static_cast<int>(rank) * per);
-    const int p1 = min(n_all, p0 + per);
+    // split attention (attention-only launches): cluster z of S takes a contiguous
+    // share of the pages, then each CTA a share of that
+    const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
+    const int zper = (n_all + S - 1) / S;
+    const int z0 = min(n_all, z * zper), z1 = min(n_all, z0 + zper);
+    const int per = (z1 - z0 + CL - 1) / CL;
+    const int p0 = min(z1, z0 + static_cast<int>(rank) * per);
+    const int p1 = min(z1, p0 + per);
 
     if (!q_staged) {
         float qv[16 * kD / kThreads];
@@ -748,6 +755,8 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     cluster_sync_all();
     // cluster merge: CTA r finalises heads r, r + CL, ...
     for (int hh = static_cast<int>(rank); hh < g; hh += CL) {
+        const int64_t qh_idx = static_cast<int64_t>(b) * a.hq + kvh * g + hh;
+        float M = -INFINITY, L = 0.f, acc = 0.f;
         if (tid < kD) {
             const float* c = sh.cpart + hh * kPartStride;
             float mr[CL], lr[CL], orr[CL];   // all remote loads in flight before any use
@@ -757,10 +766,8 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
                 lr[r] = ld_dsmem_f32(dsmem_addr(c + 1, r));
                 orr[r] = ld_dsmem_f32(dsmem_addr(c + 2 + tid, r));
             }
-            float M = -INFINITY;
 #pragma unroll
             for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, mr[r]);
-            float L = 0.f, acc = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
                 for (uint32_t r = 0; r < CL; ++r) {
@@ -770,7 +777,42 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
                     acc += orr[r] * f;
                 }
             }
-            const int64_t qh_idx = static_cast<int64_t>(b) * a.hq + kvh * g + hh;
+        }
+        if (S > 1) {
+            // this cluster's (m, l, o) of the head into the workspace; the last of the S
+            // clusters to arrive (an atomic count, no waiting) merges them
+            float* gp = a.attn_part + (qh_idx * kMaxSplits + z) * kPartStride;
+            if (tid < kD) {
+                gp[2 + tid] = acc;
+                if (tid == 0) {
+                    gp[0] = M;
+                    gp[1] = L;
+                }
+            }
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) sh.split_last = atomicAdd(&a.attn_cnt[qh_idx], 1) == S - 1;
+            __syncthreads();
+            if (!sh.split_last) continue;
+            __threadfence();
+            if (tid < kD) {
+                const float* hp = a.attn_part + qh_idx * kMaxSplits * kPartStride;
+                M = -INFINITY;
+                for (int zz = 0; zz < S; ++zz) M = fmaxf(M, __ldcg(hp + zz * kPartStride));
+                L = 0.f;
+                acc = 0.f;
+                if (M != -INFINITY) {
+                    for (int zz = 0; zz < S; ++zz) {
+                        const float mz = __ldcg(hp + zz * kPartStride);
+                        if (mz == -INFINITY) continue;
+                        const float f = fast_exp2(mz - M);
+                        L += __ldcg(hp + zz * kPartStride + 1) * f;
+                        acc += __ldcg(hp + zz * kPartStride + 2 + tid) * f;
+                    }
+                }
+            }
+        }
+        if (tid < kD) {
             const float val = (L > 0.f) ? acc / L : 0.f;
             a.out[qh_idx * kD + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
             if (a.lse && tid == 0) a.lse[qh_idx] = (L > 0.f) ? (M + fast_log2(L)) * kLn2 : -INFINITY;
@@ -871,7 +913,8 @@ cudaError_t launch_t(const SelectAttendArgs& args, cudaStream_t stream) {
     cudaError_t e = ensure_kernel_attrs<select_attend_kernel<CL, MODE, GM>>(static_cast<int>(smem), CL > 8);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL, a.batch * a.hkv, 1);
+    const int splits = (MODE == SAMode::kAttend && a.attn_part && a.attn_cnt) ? max(1, min(a.splits, kMaxSplits)) : 1;
+    cfg.gridDim = dim3(CL, a.batch * a.hkv, splits);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -244,6 +244,56 @@ def test_attention_all_pages_is_dense_attention():
             assert abs(lse_g[b, h] - (m + np.log(p.sum()))) < 1e-3
 
 
+@pytest.mark.parametrize("B,hkv,g,maxp,seq", [(1, 1, 4, 8192, [8192]), (2, 1, 4, 3000, [3000, 70]),
+                                              (1, 2, 16, 2048, [2048])])
+def test_split_attention_matches_dense_and_unsplit(B, hkv, g, maxp, seq):
+    """With a full workspace, long selections are split over several clusters per segment and
+    merged through the workspace by the last cluster to arrive: the output is the textbook
+    dense softmax, equals the unsplit launch up to the merge order, and repeats exactly."""
+    rng = np.random.default_rng(43 + maxp)
+    seq = np.array(seq, np.int32)
+    nphys = B * maxp
+    kc = synth.f32_to_bf16_bits(rng.standard_normal((nphys, hkv, 16, 128)).astype(np.float32))
+    vc = synth.f32_to_bf16_bits(rng.standard_normal((nphys, hkv, 16, 128)).astype(np.float32))
+    q = (rng.standard_normal((B, hkv * g, 128)) * 1.5).astype(np.float32)
+    table = rng.permutation(nphys).reshape(B, maxp).astype(np.int32)
+    sel = np.tile(np.arange(maxp, dtype=np.int32), (B, hkv, 1))
+    nsel = np.repeat(seq[:, None], hkv, axis=1).astype(np.int32)
+    prob = device_problem(q, kc, vc, table, seq)
+    ws = L.alloc_workspace(prob.dims, maxp * 16, DEV)
+
+    def run(workspace):
+        out = torch.zeros((B, hkv * g, 128), dtype=torch.int16, device=DEV)
+        lse = torch.zeros((B, hkv * g), dtype=torch.float32, device=DEV)
+        L.locks_sparse_attention(prob.dims, prob.q, prob.k_cache, prob.v_cache, prob.page_table, t(sel), t(nsel),
+                                 maxp, out, lse, workspace)
+        torch.cuda.synchronize()
+        return out, lse
+
+    o1, l1 = run(ws)
+    o2, l2 = run(ws)
+    assert L.locks_get_device_status(ws) == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o0, l0 = run(None)
+    assert np.abs(bf16_out(o1) - bf16_out(o0)).max() < 1e-2
+    assert np.abs(l1.cpu().numpy() - l0.cpu().numpy()).max() < 1e-4
+    got, lse_g = bf16_out(o1), l1.cpu().numpy()
+    kf = synth.bf16_bits_to_f32(kc).astype(np.float64)
+    vf = synth.bf16_bits_to_f32(vc).astype(np.float64)
+    for b in range(B):
+        phys = table[b, :seq[b]]
+        for h in range(hkv * g):
+            keys = kf[phys, h // g].reshape(-1, 128)
+            vals = vf[phys, h // g].reshape(-1, 128)
+            logits = keys @ q[b, h].astype(np.float64) / np.sqrt(128.0)
+            m = logits.max()
+            p = np.exp(logits - m)
+            ref = (p @ vals) / p.sum()
+            assert np.abs(got[b, h] - ref).max() < ATT_ABS
+            assert cosine(got[b, h], ref) >= ATT_COS
+            assert abs(lse_g[b, h] - (m + np.log(p.sum()))) < 1e-3
+
+
 # ----------------------------------------------------------- fused step
 
 def _run_decode(w, inp, mu, basis, coef, scales, budget):
