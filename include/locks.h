@@ -142,8 +142,10 @@ LOCKS_API int locks_k_cap(const locks_dims_t* dims, int32_t budget_tokens, int32
 /*
  * Workspace bytes needed by every call below for these dims and budget
  * (the decode step needs the most: the score table, its LSE partials, the
- * selection and the device status word). The workspace must be 256-byte aligned. Its first 256
- * bytes hold the status word; locks_clear_device_status zeroes it.
+ * selection and the device status word; the split partials of
+ * locks_sparse_attention share that space). The workspace must be 256-byte
+ * aligned. Its first 256 bytes hold the status word; locks_clear_device_status
+ * zeroes it. Its other contents are scratch between calls.
  */
 LOCKS_API int locks_workspace_size(const locks_dims_t* dims, int32_t budget_tokens, size_t* bytes);
 
@@ -207,6 +209,14 @@ LOCKS_API int locks_select_pages(const locks_dims_t* dims, const float* scores, 
  * read through page_table. Split-K across the CTAs of a thread-block cluster
  * per (b, kv head), merged with the online-softmax rule. k_cap is the row
  * stride of `selected`. n = 0 gives out = 0 and lse = -inf.
+ * With a workspace of at least locks_workspace_size(dims, 16 * k_cap) bytes
+ * (any workspace of locks_workspace_size for these dims suffices in practice:
+ * the split region is 256 + B*Hq*(4 + 4*130*4) bytes, rounded up), long
+ * selections (>= 64 pages per CTA) are also split over up to 4 clusters per
+ * (b, kv head) that stay co-resident; each writes its merged (m, l, o) to the
+ * workspace and the last to arrive merges them (results equal the unsplit
+ * launch up to the order of the merge). The call then zeroes the split
+ * counters with an asynchronous memset on `stream` before the launch.
  */
 LOCKS_API int locks_sparse_attention(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
                                      const uint16_t* v_cache, const int32_t* page_table,
