@@ -41,6 +41,10 @@ constexpr int kStCoef = kStBasis + kStageUnits * 512;
 constexpr int kStScales = kStCoef + kStageUnits * 128;
 constexpr int kStageBytes = kStScales + kStageUnits * 8;   // 49,664 B
 constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStages * 8;
+// Two consumer groups take alternate stages; with an even ring each group owns
+// its own slots, so its parity waits can never see a slot's phase from two fills
+// earlier (with an odd ring a group that runs ahead would).
+static_assert(kStages % 2 == 0, "the ring must hold an even number of stages");
 
 __device__ __forceinline__ float pow2i(int e) {  // 2^e for |e| <= 126
     return __int_as_float((127 + e) << 23);
