@@ -263,16 +263,29 @@ class OracleStep:
         return self.o.max_threads()
 
 
-def cpu_baseline(step: OracleStep, budget_s: float = 12.0, max_calls: int = 64) -> dict:
-    times = []
-    t_end = time.perf_counter() + budget_s
-    while len(times) < max_calls and (not times or time.perf_counter() < t_end):
-        times.append(step.run_one())
+def cpu_baseline(step: OracleStep, budget_s: float = 12.0, max_calls: int = 64, single_s: float = 4.0) -> dict:
+    def sample(seconds: float, calls: int) -> list:
+        times = []
+        t_end = time.perf_counter() + seconds
+        while len(times) < calls and (not times or time.perf_counter() < t_end):
+            times.append(step.run_one())
+        return times
+
+    cores = step.cores()
+    times = sample(budget_s, max_calls)
     per_step_us = statistics.mean(times) * step.segments * 1e6
-    return {"value": per_step_us, "unit": "us", "cores": step.cores(), "kind": "oracle",
+    # the same on one thread (a shorter bounded sample)
+    step.o.set_threads(1)
+    try:
+        single = sample(single_s, 8)
+    finally:
+        step.o.set_threads(cores)
+    return {"value": per_step_us, "unit": "us", "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} of the step's {step.segments} (request, kv head) segments, each fully "
                       f"scored/selected/attended in float64; per-step time = mean segment time x segments; "
-                      f"random summary bytes of the same shape"}
+                      f"random summary bytes of the same shape",
+            "single_thread": {"value": statistics.mean(single) * step.segments * 1e6, "unit": "us", "cores": 1,
+                              "sample": f"{len(single)} segments, extrapolated the same way"}}
 
 
 def run_reference(args, rank, world):
