@@ -16,7 +16,8 @@
 //
 // GPU mapping. Exact and variant scores: one warp per (page, kv head) unit,
 // 4 warps per CTA, one CTA per (sequence, kv head) and run of 64 pages, the
-// group's queries staged in shared memory once per CTA. The variant kernel
+// group's queries staged in shared memory once per CTA. The exact scorer runs
+// its 16 x 128 by 128 x g contraction on the tensor cores (mma.sync bf16). The variant kernel
 // keeps the unit's centred keys, Gram matrix, eigenvectors and summary in the
 // warp's own shared-memory slice and runs the cyclic Jacobi method in
 // round-robin order (8 disjoint rotations per round, 15 rounds per sweep).
@@ -110,55 +111,121 @@ __device__ __forceinline__ void stage_queries(const AblationArgs& a, int b, int 
 
 // ------------------------------------------------------------ exact scores
 
-// Grid (B * Hkv, runs of 64 pages). Lane l holds token l % 16, dims
-// [64 (l / 16), 64 (l / 16) + 64) of the unit; the two halves of each dot
-// product meet with one shuffle, then a 16-lane log-sum-exp.
+constexpr int kExSlot = kPage * kD * 2;   // one unit's 16 keys, 4 KiB
+
+// Byte offset of 16-byte chunk c (0..15) of token row r in a key slot: the chunk
+// index is XORed with the row's low bits so that ldmatrix's 8 rows of one
+// column block fall in 8 different bank groups.
+__device__ __forceinline__ int ex_swz(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_older() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// x = hi + mid + lo with each part a bf16 value (about 24 significant bits in all).
+__device__ __forceinline__ void split3_bf16(float x, float& hi, float& mid, float& lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    const float r = x - hi;
+    mid = __bfloat162float(__float2bfloat16_rn(r));
+    lo = __bfloat162float(__float2bfloat16_rn(r - mid));
+}
+
+// Grid (B * Hkv, runs of 64 pages); HT = ceil(g / 8) tiles of 8 heads. One warp per
+// unit: the unit's keys (exactly bf16) are copied into the warp's slot (cp.async,
+// double-buffered: the next unit's copy runs while this one is scored) and are the
+// A operand of mma.sync m16n8k16 bf16 (rows = the 16 tokens, k = dims, through
+// ldmatrix); B = the queries of 8 heads, each split into three bf16 parts that are
+// separate MMAs, summed in fp32, so the logits carry fp32-accurate products. The
+// page LSE is taken on the accumulator layout (each lane holds two heads' logits
+// of tokens gid and gid + 8).
+template <int HT>
 __global__ void __launch_bounds__(kAbWarps * 32) exact_kernel(AblationArgs a) {
-    extern __shared__ float qs[];
+    extern __shared__ __align__(128) unsigned char ex_smem[];
     const int g = a.hq / a.hkv;
     const int b = blockIdx.x / a.hkv, kvh = blockIdx.x % a.hkv;
     const int P = seq_len(a, b);
     const int j0 = blockIdx.y * kAbPagesPerCta;
     if (j0 >= P) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, t = lane & 3;
+    uint8_t* slots = ex_smem + warp * 2 * kExSlot;
+    float* qs = reinterpret_cast<float*>(ex_smem + kAbWarps * 2 * kExSlot);
     stage_queries(a, b, kvh, qs);
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok = lane & 15, half = lane >> 4;
-    const int j1 = min(P, j0 + kAbPagesPerCta);
-    auto load_unit = [&](int j, uint4 (&dst)[8]) {
-        const int64_t phys = phys_page(a, b, j);
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.k_cache + ((phys * a.hkv + kvh) * kPage + tok) * kD + half * 64);
+    // B fragments: head ht * 8 + gid, dims 16 ks + 2t (+1) and 16 ks + 2t + 8 (+9)
+    uint32_t bq[HT][3][8][2];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) dst[v] = src[v];
-    };
-    uint4 nxt[8];   // the warp's next unit, loaded while the current one is scored
-    if (j0 + warp < j1) load_unit(j0 + warp, nxt);
-    for (int j = j0 + warp; j < j1; j += kAbWarps) {
-        float k[64];
+    for (int ht = 0; ht < HT; ++ht) {
+        const int head = ht * 8 + gid;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) bf16x8_to_f32(nxt[v], k + 8 * v);
-        if (j + kAbWarps < j1) load_unit(j + kAbWarps, nxt);
-        for (int hh = 0; hh < g; ++hh) {
-            const float4* qv = reinterpret_cast<const float4*>(qs + hh * kD + half * 64);
-            float d0 = 0.f, d1 = 0.f;
+        for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-            for (int c = 0; c < 16; c += 2) {
-                const float4 x = qv[c], y = qv[c + 1];
-                d0 = fmaf(x.x, k[4 * c], d0);
-                d0 = fmaf(x.y, k[4 * c + 1], d0);
-                d0 = fmaf(x.z, k[4 * c + 2], d0);
-                d0 = fmaf(x.w, k[4 * c + 3], d0);
-                d1 = fmaf(y.x, k[4 * c + 4], d1);
-                d1 = fmaf(y.y, k[4 * c + 5], d1);
-                d1 = fmaf(y.z, k[4 * c + 6], d1);
-                d1 = fmaf(y.w, k[4 * c + 7], d1);
+            for (int half = 0; half < 2; ++half) {
+                const int d = 16 * ks + 2 * t + 8 * half;
+                const float x0 = head < g ? qs[head * kD + d] : 0.f;
+                const float x1 = head < g ? qs[head * kD + d + 1] : 0.f;
+                float h0, m0, l0, h1, m1, l1;
+                split3_bf16(x0, h0, m0, l0);
+                split3_bf16(x1, h1, m1, l1);
+                bq[ht][0][ks][half] = pack_bf16x2(h0, h1);
+                bq[ht][1][ks][half] = pack_bf16x2(m0, m1);
+                bq[ht][2][ks][half] = pack_bf16x2(l0, l1);
             }
-            float d = d0 + d1;
-            d += __shfl_xor_sync(0xffffffffu, d, 16);
-            const float s = lse16_log2(d * (kInvSqrtD * kLog2e));
-            if (lane == 0) a.scores[(static_cast<int64_t>(b) * a.hq + kvh * g + hh) * a.max_pages + j] = s;
+    }
+    const int j1 = min(P, j0 + kAbPagesPerCta);
+    auto issue = [&](int j, int slot) {
+        const int64_t phys = phys_page(a, b, j);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.k_cache + (phys * a.hkv + kvh) * kPage * kD);
+        uint8_t* dst = slots + slot * kExSlot;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = lane + 32 * i;   // 16-byte chunk c of the unit: token c / 16, chunk c % 16
+            cp_async_16(dst + ex_swz(c >> 4, c & 15), src + c * 16);
         }
+    };
+    if (j0 + warp < j1) issue(j0 + warp, 0);
+    cp_async_commit();
+    int slot = 0;
+    for (int j = j0 + warp; j < j1; j += kAbWarps) {
+        if (j + kAbWarps < j1) issue(j + kAbWarps, slot ^ 1);
+        cp_async_commit();
+        cp_async_wait_older();   // this unit's copy has landed
+        __syncwarp();
+        const uint8_t* kb = slots + slot * kExSlot;
+        float acc[HT][3][4];
+#pragma unroll
+        for (int ht = 0; ht < HT; ++ht)
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp) acc[ht][sp][0] = acc[ht][sp][1] = acc[ht][sp][2] = acc[ht][sp][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t af[4];   // rows 0-7 / 8-15 x dims 16 ks .. +7 / 16 ks + 8 .. +15
+            ldmatrix_x4(af, kb + ex_swz((lane & 7) + 8 * ((lane >> 3) & 1), 2 * ks + (lane >> 4)));
+#pragma unroll
+            for (int ht = 0; ht < HT; ++ht)
+#pragma unroll
+                for (int sp = 0; sp < 3; ++sp) mma_bf16_16816(acc[ht][sp], af, bq[ht][sp][ks][0], bq[ht][sp][ks][1]);
+        }
+#pragma unroll
+        for (int ht = 0; ht < HT; ++ht) {
+#pragma unroll
+            for (int col = 0; col < 2; ++col) {   // head ht * 8 + 2t + col: tokens gid (e = col), gid + 8 (e = col + 2)
+                const float xa = ((acc[ht][0][col] + acc[ht][1][col]) + acc[ht][2][col]) * (kInvSqrtD * kLog2e);
+                const float xb =
+                    ((acc[ht][0][col + 2] + acc[ht][1][col + 2]) + acc[ht][2][col + 2]) * (kInvSqrtD * kLog2e);
+                float m = fmaxf(xa, xb);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                float z = fast_exp2(xa - m) + fast_exp2(xb - m);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                const int head = ht * 8 + 2 * t + col;
+                if (gid == 0 && head < g)
+                    a.scores[(static_cast<int64_t>(b) * a.hq + kvh * g + head) * a.max_pages + j] =
+                        (m + fast_log2(z)) * kLn2;
+            }
+        }
+        __syncwarp();   // every lane is done with the slot before it is refilled
+        slot ^= 1;
     }
 }
 
@@ -606,8 +673,13 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(AblationArgs a) {
 
 cudaError_t launch_exact_scores(const AblationArgs& a, cudaStream_t stream) {
     if (a.batch == 0 || a.max_pages == 0) return cudaSuccess;
+    const int g = a.hq / a.hkv;
     const dim3 grid(a.batch * a.hkv, (a.max_pages + kAbPagesPerCta - 1) / kAbPagesPerCta);
-    exact_kernel<<<grid, kAbWarps * 32, (a.hq / a.hkv) * kD * 4, stream>>>(a);
+    const int smem = kAbWarps * 2 * kExSlot + g * kD * 4;   // at most 40 KiB (g <= 16)
+    if (g <= 8)
+        exact_kernel<1><<<grid, kAbWarps * 32, smem, stream>>>(a);
+    else
+        exact_kernel<2><<<grid, kAbWarps * 32, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
