@@ -492,6 +492,18 @@ def run_locks(args, rank, world, local):
         one = ids[:1].clone()                                        # physical page 0
         fresh = L.Summaries.empty(1, w.num_kv_heads, dev)            # its new summary (not read by the step)
         L.locks_build_summaries(dims, kc, one, 1, fresh)
+        # the step a caller runs while pages fill: locks_decode_step_tail (no tail tokens here),
+        # whose scorer leaves one SM to the concurrent one-page builds
+        tails = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+
+        def tail_step():
+            L.locks_decode_step(dims, q, kc, vc, summ, table, seq, budget, out, ws, lse=lse, tail_tokens=tails)
+
+        tail_step()
+        torch.cuda.synchronize()
+        g_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_tail):
+            tail_step()
         torch.cuda.synchronize()
         alone, with_refresh, plain = [], [], []
         for i in range(12):
@@ -510,8 +522,7 @@ def run_locks(args, rank, world, local):
                 c_, d_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 c_.record(stream)
                 for k in range(3):
-                    g_score.replay()
-                    g_sa.replay()
+                    g_tail.replay()
                     if with_build and k == 0:
                         side.wait_stream(stream)
                         with torch.cuda.stream(side):
@@ -526,10 +537,12 @@ def run_locks(args, rank, world, local):
                    "three_steps_with_refresh_us": statistics.mean(with_refresh),
                    "refresh_cost_us": statistics.mean(with_refresh) - statistics.mean(plain),
                    "samples": len(alone),
+                   "tail_step_us": statistics.mean(plain) / 3.0,
                    "path": "locks_build_summaries(n_pages=1) for a page that just filled, on a second stream, "
                            "launched after the first of three consecutive steps is queued (the page stays in "
-                           "the tail, attended whole, until the build completes); refresh_cost_us = the "
-                           "three steps' extra time"}
+                           "the tail, attended whole, until the build completes); the steps are "
+                           "locks_decode_step_tail in one graph each (its scorer leaves one SM to the build); "
+                           "refresh_cost_us = the three steps' extra time"}
         assert L.locks_get_device_status(ws) == 0, "device status after the refresh timing"
 
     # dense comparator (outside the timed region): the same attention kernel with every page

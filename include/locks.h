@@ -267,7 +267,9 @@ LOCKS_API int locks_decode_step(const locks_dims_t* dims, const float* q, const 
  * Page-fill refresh: when a page fills, the caller launches locks_build_summaries
  * for it (n_pages = 1) on another stream and keeps its 16 tokens in the tail
  * until that build has completed; then it advances seq_pages[b] by one and
- * takes 16 off tail_tokens[b].
+ * takes 16 off tail_tokens[b]. With tail_tokens given, locks_decode_step_tail
+ * runs its persistent scorer on one SM fewer than the GPU has, leaving that SM
+ * to such a build (one CTA) instead of having a scorer CTA wait for it.
  */
 LOCKS_API int locks_select_attend_tail(const locks_dims_t* dims, const float* q, const uint16_t* k_cache,
                                        const uint16_t* v_cache, const int32_t* page_table, const float* scores,

@@ -182,8 +182,10 @@ bool select_fits(int max_pages, locks::SAMode mode) {
     return locks::select_attend_smem_bytes(max_pages, 8, mode) <= 200 * 1024;
 }
 
+// reserve_sms: SMs the persistent scorer leaves free (for concurrent one-page builds).
 int score_impl(const locks_dims_t* dims, const float* q, locks_summaries_t s, const int32_t* page_table,
-               const int32_t* seq_pages, float* scores, float* partials, void* ws, cudaStream_t stream) {
+               const int32_t* seq_pages, float* scores, float* partials, void* ws, cudaStream_t stream,
+               int reserve_sms = 0) {
     const int dev = current_device();
     if (dev < 0) return LOCKS_ERR_CUDA;
     locks::ScoreArgs a;
@@ -202,7 +204,7 @@ int score_impl(const locks_dims_t* dims, const float* q, locks_summaries_t s, co
     a.max_pages = dims->max_pages_per_seq;
     a.num_phys = dims->num_phys_pages;
     a.st = status_of(ws);
-    return cuda_status(locks::launch_score(a, num_sms(dev), stream));
+    return cuda_status(locks::launch_score(a, std::max(1, num_sms(dev) - reserve_sms), stream));
 }
 
 locks::SelectAttendArgs sa_args(const locks_dims_t* dims, void* ws) {
@@ -444,7 +446,10 @@ int locks_decode_step_tail(const locks_dims_t* dims, const float* q, const uint1
     float* partials = reinterpret_cast<float*>(base + L.partials);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dims->max_pages_per_seq > 0) {
-        v = score_impl(dims, q, summaries, page_table, seq_pages, scores, partials, workspace, st);
+        // with tails, pages are being filled and their one-page builds run on another
+        // stream: leave them an SM rather than have one scorer CTA wait for it
+        v = score_impl(dims, q, summaries, page_table, seq_pages, scores, partials, workspace, st,
+                       tail_tokens ? 1 : 0);
         if (v != LOCKS_OK) return v;
     }
     return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, partials, seq_pages, tail_tokens,
