@@ -112,3 +112,30 @@ def test_full_size_decode_step(wname, budget):
     assert np.abs(got - ref_o)[heads].max() < ATT_ABS
     assert cosine(got, ref_o)[heads].min() >= ATT_COS
     assert np.abs(lse.cpu().numpy() - ref_l)[heads].max() < 1e-3
+
+
+def test_full_size_dense_attention_split_over_clusters():
+    """The dense comparator's launch at 1M context (8 segments, each split over several
+    clusters and merged through the workspace, every one of 65,536 pages selected) against
+    the oracle's attention over all 1M tokens of every head. K and V come from a pool of
+    2,048 random pages that a pseudo-random page table maps every logical page onto."""
+    rng = np.random.default_rng(77)
+    B, Hq, Hkv, P, pool = 1, 32, 8, 65536, 2048
+    kc = synth.f32_to_bf16_bits(rng.standard_normal((pool, Hkv, 16, 128)).astype(np.float32))
+    vc = synth.f32_to_bf16_bits(rng.standard_normal((pool, Hkv, 16, 128)).astype(np.float32))
+    q = (rng.standard_normal((B, Hq, 128)) * 2.0).astype(np.float32)
+    table = ((np.arange(P, dtype=np.int64) * 7919 + 13) % pool).astype(np.int32)[None]
+    sel = np.tile(np.arange(P, dtype=np.int32), (B, Hkv, 1))
+    nsel = np.full((B, Hkv), P, np.int32)
+    dims = L.make_dims(B, Hq, Hkv, P, pool)
+    ws = L.alloc_workspace(dims, 2048, DEV)              # the decode step's workspace, as in the bench
+    out = torch.zeros((B, Hq, 128), dtype=torch.int16, device=DEV)
+    lse = torch.zeros((B, Hq), dtype=torch.float32, device=DEV)
+    L.locks_sparse_attention(dims, t(q), t(kc), t(vc), t(table), t(sel), t(nsel), P, out, lse, ws)
+    torch.cuda.synchronize()
+    assert L.locks_get_device_status(ws) == 0
+    ref_o, ref_l = oracle.attend(q, kc, vc, table, sel, nsel)
+    got = bf16_out(out)
+    assert np.abs(got - ref_o).max() < ATT_ABS
+    assert cosine(got, ref_o).min() >= ATT_COS
+    assert np.abs(lse.cpu().numpy() - ref_l).max() < 1e-3
