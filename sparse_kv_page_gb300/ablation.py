@@ -10,7 +10,12 @@ summary, sections 1 and 3):
 * mass          - sum over the chosen pages of the exact group-mean attention
                   share (each segment's shares sum to 1), averaged; the exact
                   selection's own value is the most any k pages can hold;
-* carriers_kept - fraction of the planted carrier pages chosen.
+* carriers_kept - fraction of the planted carrier pages chosen;
+* eta           - the largest |score - exact score| over (head, page), with the
+                  mean error and e^(-4 eta), the least share of the best attainable
+                  mass Theorem 1 guarantees an unquantised summary's selection
+                  (gist.science summary, section 3), beside mass_vs_exact, the share
+                  actually kept.
 
 Selectors: the shipped rank-8 int8/int4/int8 summary (built once, scored by
 locks_score_pages), page-local summaries of other ranks and code widths
@@ -26,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 from typing import Callable, Dict, List, Sequence
 
@@ -104,6 +110,7 @@ def run(dims, q, k_cache, page_table, seq_pages, summaries, budget: int, carrier
 
     exact_us = _time_us(exact)
     exact()
+    exact_scores = scores.clone()
     mem_e = select(with_keys=True)
     live = torch.arange(P, device=device)[None, None, :] < seq_pages.long()[:, None, None]
     share = torch.where(live, torch.exp(keys.double()), torch.zeros((), dtype=torch.float64, device=device))
@@ -112,10 +119,18 @@ def run(dims, q, k_cache, page_table, seq_pages, summaries, budget: int, carrier
     n_car = int(cmask.sum().item())
 
     def row(name: str, mem: torch.Tensor, us: float, **extra) -> Dict:
+        # eta: the largest |score - exact score| over (head, page) (Theorem 1's error; the
+        # selection keeps at least e^(-4 eta) of the best attainable mass, unquantised summaries)
+        err = torch.where(live, (scores - exact_scores).abs(), torch.zeros((), device=device))
+        eta = float(err.max().item())
         r = {"selector": name,
              "recall": round(float(((mem & mem_e).sum(2).double() / n_e).mean().item()), 4),
              "mass": round(float((share * mem).sum(2).mean().item()), 4),
+             "mass_vs_exact": round(float(((share * mem).sum(2) / (share * mem_e).sum(2)).mean().item()), 4),
              "carriers_kept": round(float((mem & cmask).sum().item()) / max(n_car, 1), 4),
+             "eta": round(eta, 4),
+             "mean_score_err": round(float(err.sum().item() / (live.sum().item() * hq)), 5),
+             "theorem1_bound": round(math.exp(-4.0 * eta), 4),
              "score_us": round(us, 1)}
         r.update(extra)
         return r

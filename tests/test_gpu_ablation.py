@@ -226,6 +226,12 @@ def test_ablation_harness_properties():
         assert 0.0 <= r["recall"] <= 1.0 and 0.0 <= r["carriers_kept"] <= 1.0
         assert r["mass"] <= exact["mass"] + 1e-4, r
     assert rows["r15 unquantised"]["recall"] >= 0.99
+    assert exact["eta"] == 0.0 and exact["mass_vs_exact"] == 1.0
+    for r in rec["rows"]:
+        if r["selector"].startswith("r") and r.get("bits") == [0, 0, 0]:
+            # Theorem 1: an unquantised summary's selection keeps at least e^(-4 eta) of the best mass
+            assert r["mass_vs_exact"] >= r["theorem1_bound"] - 1e-4, r
+    assert rows["r15 unquantised"]["eta"] < 1e-3
     shipped = rows["r8 int8/int4/int8 (shipped summary, locks_score_pages)"]
     variant = rows["r8 int8/int4/int8 (variant kernel)"]
     assert abs(shipped["recall"] - variant["recall"]) <= 0.02
