@@ -268,26 +268,6 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                            __half2float(__ushort_as_half(static_cast<unsigned short>(sc.y & 0xffffu))) *
                            (kInvSqrtD * kLog2e);
                 }
-                // centroid term: rows = the warp's 8 units, K = 128 dims
-                float accmu[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) accmu[nt][0] = accmu[nt][1] = accmu[nt][2] = accmu[nt][3] = 0.f;
-                {
-                    const uint8_t* mrow = stg + kStMu + (ubase + gid * HKV) * 128 + t * 32;
-                    const uint4 m0 = *reinterpret_cast<const uint4*>(mrow);
-                    const uint4 m1 = *reinterpret_cast<const uint4*>(mrow + 16);
-                    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        uint32_t lo, hi;
-                        int8x4_to_f16x2_sub(mw[ks], lo, hi);
-                        const uint32_t af[4] = {lo, 0u, hi, 0u};
-                        // B rows d + 8, d + 9 back to full size (x16) for the int8 codes
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_f16_16816(accmu[nt], af, bq[ks][nt][0], hmul2_u32(bq[ks][nt][1], 0x4c004c00u));
-                    }
-                }
                 const float smu_row = __shfl_sync(0xffffffffu, s_mu, gid);
                 // Per-token logits (log2 domain) of units i and i + 4: MMA1 gives V^T q for both
                 // (rows 0-7 and 8-15), MMA2 reconstructs the 16 tokens of each; `use(u, nt, x0, x1)`
@@ -385,6 +365,27 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                             z += __shfl_xor_sync(0xffffffffu, z, 16);
                             if (gid == u) lse[nt] = (m + fast_log2(z)) * kLn2;
                         });
+                }
+                // centroid term: rows = the warp's 8 units, K = 128 dims (taken after the
+                // token logits so that its accumulators are not live across them)
+                float accmu[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) accmu[nt][0] = accmu[nt][1] = accmu[nt][2] = accmu[nt][3] = 0.f;
+                {
+                    const uint8_t* mrow = stg + kStMu + (ubase + gid * HKV) * 128 + t * 32;
+                    const uint4 m0 = *reinterpret_cast<const uint4*>(mrow);
+                    const uint4 m1 = *reinterpret_cast<const uint4*>(mrow + 16);
+                    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint32_t lo, hi;
+                        int8x4_to_f16x2_sub(mw[ks], lo, hi);
+                        const uint32_t af[4] = {lo, 0u, hi, 0u};
+                        // B rows d + 8, d + 9 back to full size (x16) for the int8 codes
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_f16_16816(accmu[nt], af, bq[ks][nt][0], hmul2_u32(bq[ks][nt][1], 0x4c004c00u));
+                    }
                 }
                 // score of unit gid, head 4 nt + t: centroid term + token LSE
                 float score_out[NT];
