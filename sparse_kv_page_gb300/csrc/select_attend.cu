@@ -130,8 +130,11 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
                 x[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : -INFINITY;
         }
     };
-    float v[kB][GM];
+    // the first two batches of scores are in flight during the normaliser below, and
+    // two stay in flight in the key loop
+    float v[kB][GM], v2[kB][GM];
     load_batch(v, j0 + tid);
+    load_batch(v2, j0 + tid + kStep);
     float qv[16 * kD / kThreads];
     if (stage_q) load_query(a, b, kvh, g, qv);
 
@@ -168,6 +171,11 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
                 for (int u = 0; u < kB; ++u)
 #pragma unroll
                     for (int hh = 0; hh < GM; ++hh) x[u][hh] = v[u][hh];
+            } else if (jb == j0 + tid + kStep) {
+#pragma unroll
+                for (int u = 0; u < kB; ++u)
+#pragma unroll
+                    for (int hh = 0; hh < GM; ++hh) x[u][hh] = v2[u][hh];
             } else {
                 load_batch(x, jb);
             }
@@ -248,8 +256,8 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
 #pragma unroll 1
     for (int jb = j0 + tid; jb < j1; jb += kStep) {
         float w[kB][GM];
-        const bool more = jb + kStep < j1;
-        if (more) load_batch(w, jb + kStep);   // next batch in flight while this one is used
+        const bool more = jb + 2 * kStep < j1;
+        if (more) load_batch(w, jb + 2 * kStep);   // two batches in flight while this one is used
 #pragma unroll
         for (int u = 0; u < kB; ++u) {
             const int j = jb + u * kThreads;
@@ -278,12 +286,13 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
                 if (a.sel_keys) a.sel_keys[(static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages + j] = key;
             }
         }
-        if (more) {
 #pragma unroll
-            for (int u = 0; u < kB; ++u)
+        for (int u = 0; u < kB; ++u)
 #pragma unroll
-                for (int hh = 0; hh < GM; ++hh) v[u][hh] = w[u][hh];
-        }
+            for (int hh = 0; hh < GM; ++hh) {
+                v[u][hh] = v2[u][hh];
+                if (more) v2[u][hh] = w[u][hh];
+            }
     }
     __syncthreads();
 }
