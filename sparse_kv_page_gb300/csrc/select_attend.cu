@@ -3,7 +3,10 @@
 // One thread-block cluster of CL CTAs per (sequence b, kv head). The CTAs of
 // a cluster split the sequence's pages (selection) and then the selected
 // pages (attention) and combine their partial results through distributed
-// shared memory, so no global scratch and no second launch is needed.
+// shared memory, so selection and attention need no global scratch and no
+// second launch. Attention-only launches over long selections may also split
+// a (sequence, kv head) over several clusters, merged through the workspace
+// by the last cluster to finish.
 //
 // Selection (gist.science summary of the LOCKS paper, 2.3 "group-shared
 // selection"; LOCKS post, "Code": keep budget // 16 pages, sorted ascending):
@@ -15,10 +18,10 @@
 //   is written in ascending page order by an ordered compaction.
 // Attention (LOCKS post, "Code": scaled dot-product attention over the pages
 // kept): each CTA takes a contiguous share of the selected pages; each warp
-// streams one page at a time (16 K rows + 16 V rows, 256-byte bulk copies
-// into padded shared rows) and runs QK^T and PV on the tensor cores
-// (mma.sync bf16, query split hi/lo, online softmax in fp32). Warp partials
-// (m, l, o) are merged per CTA, then across the cluster.
+// streams one page at a time (its K and V rows as four tiled TMA boxes of 16
+// tokens x 64 dims, 128-byte swizzle) and runs QK^T and PV on the tensor cores
+// (mma.sync bf16 through ldmatrix, query split hi/lo, online softmax in fp32).
+// Warp partials (m, l, o) are merged per CTA, then across the cluster.
 //
 // When the scoring kernel's per-8-page LSE partials are given, the per-head
 // normaliser L_h is reduced from them instead of from the full score table.
