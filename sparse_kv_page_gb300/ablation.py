@@ -87,6 +87,31 @@ def carrier_mask(carriers: Sequence[Sequence[np.ndarray]], shape, device) -> tor
     return m
 
 
+def selection_metrics(mem: torch.Tensor, mem_exact: torch.Tensor, share: torch.Tensor, carriers: torch.Tensor,
+                      scores: torch.Tensor, exact_scores: torch.Tensor, live: torch.Tensor) -> Dict:
+    """The metrics of one selector against the exact selection.
+
+    mem, mem_exact, carriers: bool [B][Hkv][P] (chosen pages, the exact selection's,
+    the planted carriers); share: float64 [B][Hkv][P], each (request, kv head)'s exact
+    group-mean attention shares (zero past the sequence); scores, exact_scores:
+    [B][Hq][P] page scores of the selector and of the exact selector; live: bool
+    [B][1][P], the sequence's pages.
+    """
+    n_e = mem_exact.sum(2).clamp(min=1).double()
+    held = (share * mem).sum(2)
+    err = torch.where(live, (scores - exact_scores).abs(), torch.zeros((), dtype=scores.dtype, device=scores.device))
+    eta = float(err.max().item()) if err.numel() else 0.0
+    n_live = int(live.sum().item()) * scores.shape[1]
+    n_car = int(carriers.sum().item())
+    return {"recall": round(float(((mem & mem_exact).sum(2).double() / n_e).mean().item()), 4),
+            "mass": round(float(held.mean().item()), 4),
+            "mass_vs_exact": round(float((held / (share * mem_exact).sum(2)).mean().item()), 4),
+            "carriers_kept": round(float((mem & carriers).sum().item()) / max(n_car, 1), 4),
+            "eta": round(eta, 4),
+            "mean_score_err": round(float(err.sum().item()) / max(n_live, 1), 5),
+            "theorem1_bound": round(math.exp(-4.0 * eta), 4)}
+
+
 def run(dims, q, k_cache, page_table, seq_pages, summaries, budget: int, carriers, device,
         variants=VARIANTS, shared_ranks=SHARED_RANKS) -> Dict:
     """All selectors on one resident configuration; returns the ablation record."""
@@ -114,24 +139,15 @@ def run(dims, q, k_cache, page_table, seq_pages, summaries, budget: int, carrier
     mem_e = select(with_keys=True)
     live = torch.arange(P, device=device)[None, None, :] < seq_pages.long()[:, None, None]
     share = torch.where(live, torch.exp(keys.double()), torch.zeros((), dtype=torch.float64, device=device))
-    n_e = mem_e.sum(2).clamp(min=1).double()
     cmask = carrier_mask(carriers, (B, hkv, P), device)
     n_car = int(cmask.sum().item())
 
     def row(name: str, mem: torch.Tensor, us: float, **extra) -> Dict:
         # eta: the largest |score - exact score| over (head, page) (Theorem 1's error; the
         # selection keeps at least e^(-4 eta) of the best attainable mass, unquantised summaries)
-        err = torch.where(live, (scores - exact_scores).abs(), torch.zeros((), device=device))
-        eta = float(err.max().item())
-        r = {"selector": name,
-             "recall": round(float(((mem & mem_e).sum(2).double() / n_e).mean().item()), 4),
-             "mass": round(float((share * mem).sum(2).mean().item()), 4),
-             "mass_vs_exact": round(float(((share * mem).sum(2) / (share * mem_e).sum(2)).mean().item()), 4),
-             "carriers_kept": round(float((mem & cmask).sum().item()) / max(n_car, 1), 4),
-             "eta": round(eta, 4),
-             "mean_score_err": round(float(err.sum().item() / (live.sum().item() * hq)), 5),
-             "theorem1_bound": round(math.exp(-4.0 * eta), 4),
-             "score_us": round(us, 1)}
+        r = {"selector": name}
+        r.update(selection_metrics(mem, mem_e, share, cmask, scores, exact_scores, live))
+        r["score_us"] = round(us, 1)
         r.update(extra)
         return r
 

@@ -37,3 +37,23 @@ def test_carrier_mask():
     m = AB.carrier_mask(carriers, (2, 2, 5), "cpu")
     assert m.sum().item() == 5
     assert m[0, 0, 1] and m[0, 0, 4] and m[1, 0, 0] and m[1, 1, 2] and m[1, 1, 3]
+
+
+def test_selection_metrics_hand_worked():
+    """One (request, kv head) of 4 pages, 2 query heads: every metric by hand."""
+    import math
+    share = torch.tensor([[[0.4, 0.3, 0.2, 0.1]]], dtype=torch.float64)
+    exact_sel = torch.tensor([[[True, True, False, False]]])
+    chosen = torch.tensor([[[True, False, True, False]]])
+    carriers = torch.tensor([[[False, True, True, False]]])
+    exact_scores = torch.zeros((1, 2, 4))
+    scores = torch.tensor([[[0.0, 0.5, -0.25, 0.0], [0.1, 0.0, 0.0, 9.0]]])
+    live = torch.tensor([[[True, True, True, False]]])        # page 3 is past the sequence
+    m = AB.selection_metrics(chosen, exact_sel, share, carriers, scores, exact_scores, live)
+    assert m["recall"] == 0.5                                 # {0} of {0, 1}
+    assert m["mass"] == 0.6                                   # 0.4 + 0.2
+    assert m["mass_vs_exact"] == round(0.6 / 0.7, 4)
+    assert m["carriers_kept"] == 0.5                          # page 2 of {1, 2}
+    assert m["eta"] == 0.5                                    # page 3's 9.0 is not live
+    assert m["mean_score_err"] == round((0.5 + 0.25 + 0.1) / 6, 5)
+    assert m["theorem1_bound"] == round(math.exp(-2.0), 4)
