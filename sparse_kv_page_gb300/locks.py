@@ -5,6 +5,21 @@ same name in ``liblocks_gb300.so`` with raw device pointers taken from torch
 tensors, on torch's current CUDA stream unless a stream is given. Nothing here
 computes any part of the method, and there is no fallback: if the library is
 missing or a call fails, an exception is raised.
+
+A decode step over a paged cache (bf16 bits held in int16 tensors)::
+
+    dims = make_dims(B, Hq, Hkv, max_pages, num_phys)
+    summ = Summaries.empty(num_phys, Hkv)                  # resident summaries
+    locks_build_summaries(dims, k_cache, page_ids, n, summ)  # when pages fill
+    ws = alloc_workspace(dims, budget_tokens)
+    out = torch.empty((B, Hq, 128), dtype=torch.int16, device="cuda")
+    locks_decode_step(dims, q, k_cache, v_cache, summ, page_table, seq_pages,
+                      budget_tokens, out, ws)               # graph-capturable
+    assert locks_get_device_status(ws) == LOCKS_OK
+
+q is fp32 [B][Hq][128]; k_cache / v_cache are [num_phys][Hkv][16][128];
+page_table int32 [B][max_pages]; seq_pages int32 [B] (full, summarised pages);
+out receives bf16 bits [B][Hq][128].
 """
 
 from __future__ import annotations
