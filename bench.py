@@ -263,6 +263,26 @@ class OracleStep:
         return self.o.max_threads()
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline record."""
+    import subprocess
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(step: OracleStep, budget_s: float = 12.0, max_calls: int = 64, single_s: float = 4.0) -> dict:
     def sample(seconds: float, calls: int) -> list:
         times = []
@@ -280,7 +300,7 @@ def cpu_baseline(step: OracleStep, budget_s: float = 12.0, max_calls: int = 64, 
         single = sample(single_s, 8)
     finally:
         step.o.set_threads(cores)
-    return {"value": per_step_us, "unit": "us", "cores": cores, "kind": "oracle",
+    return {"value": per_step_us, "unit": "us", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{len(times)} of the step's {step.segments} (request, kv head) segments, each fully "
                       f"scored/selected/attended in float64; per-step time = mean segment time x segments; "
                       f"random summary bytes of the same shape",
@@ -303,6 +323,7 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, budget),
             "cpu_baseline": {"value": value, "unit": "us", "cores": step.cores(), "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"each step = one (request, kv head) segment of {step.segments}, "
                                        f"extrapolated x{step.segments}"},
             "e2e": {"value": value, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -439,18 +460,32 @@ def run_locks(args, rank, world, local):
     q_host = torch.from_numpy(np.ascontiguousarray(synth.make_queries(w))).pin_memory()
     out_host = torch.empty(out.shape, dtype=torch.int16).pin_memory()
     n_e2e = min(K, 200)
-    e2e_us = []
-    for i in range(n_e2e + 3):
-        flush.zero_()
-        torch.cuda.synchronize()
-        t1 = time.perf_counter()
+
+    def e2e_step():
         q.copy_(q_host, non_blocking=True)
         L.locks_decode_step(dims, q, kc, vc, summ, table, seq, budget, out, ws, lse=lse)
         out_host.copy_(out, non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= 3:
-            e2e_us.append((time.perf_counter() - t1) * 1e6)
+
+    # the step as a serving loop runs it: copy-in, the decode step and copy-out captured in one
+    # CUDA graph (the library's calls are graph-capturable), replayed and synchronised per step;
+    # and the same three calls issued eagerly through the C ABI each step
+    e2e_step()
+    torch.cuda.synchronize()
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e):
+        e2e_step()
+    e2e_us, e2e_eager_us = [], []
+    for run, acc in ((g_e2e.replay, e2e_us), (e2e_step, e2e_eager_us)):
+        for i in range(n_e2e + 3):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t1 = time.perf_counter()
+            run()
+            torch.cuda.synchronize()
+            if i >= 3:
+                acc.append((time.perf_counter() - t1) * 1e6)
     e2e_value = reduce_max(statistics.mean(e2e_us), world, dev)
+    e2e_eager = reduce_max(statistics.mean(e2e_eager_us), world, dev)
 
     # full-model decode graph (outside the timed region): 32 layers' decode steps (score +
     # select_attend each) in one CUDA graph, each layer streaming the same resident buffers
@@ -628,7 +663,10 @@ def run_locks(args, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "us", "h2d_bytes_per_step": int(q_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host.numel() * 2),
-                "path": "pinned q -> locks_decode_step -> output to pinned host, synchronised, wall clock"},
+                "path": "pinned q -> locks_decode_step -> output to pinned host, the three captured in one CUDA "
+                        "graph, replayed and synchronised each step, wall clock",
+                "eager_us": e2e_eager, "eager_path": "the same three calls issued eagerly through the C ABI "
+                                                    "(ctypes) each step, synchronised, wall clock"},
         "launch": "timed steps: one CUDA graph per step (score_pages, then select_attend launched "
                   "programmatically dependent on it), L2 flushed before each; kernels_us: a second pass of "
                   "K steps with one graph per kernel and an event between them",

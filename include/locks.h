@@ -296,10 +296,14 @@ LOCKS_API int locks_decode_step_tail(const locks_dims_t* dims, const float* q, c
  * exits. The caller still passes all inputs and outputs (out, and lse which
  * may be NULL).
  * - Returns LOCKS_ERR_WORKSPACE_TOO_SMALL when locks_workspace_size(dims,
- *   budget_tokens) exceeds 36 MiB (for example batch 4 x 32 query heads x
- *   65536 pages fits; batch 8 at the same sizes does not).
- * - The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   budget_tokens) exceeds 36 MiB. The score table (4 bytes) and its LSE
+ *   partials (1 byte) per (sequence, query head, page) dominate: at 32 query
+ *   heads and 65536 pages (1M tokens) each sequence needs 10 MiB, so batch 3
+ *   fits (30 MiB) and batch 4 (40 MiB) is rejected.
+ * - The first call in each CUDA context (per device) looks up the array's
+ *   device address with that device current and caches it for that context;
+ *   make that first call before any stream capture. Resetting the device
+ *   (cudaDeviceReset) after that first call is not supported.
  * - All calls share the one array and it keeps the last call's contents:
  *   calls that overlap on the GPU (other streams, other threads) race and
  *   must be serialised by the caller.

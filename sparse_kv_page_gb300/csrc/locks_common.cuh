@@ -87,15 +87,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-// Global -> shared bulk copy (TMA engine), completion counted on `bar` in bytes.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                               uint64_t policy) {
     asm volatile(
@@ -172,26 +163,6 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-// Eight int4 codes (two's complement nibbles n0..n7 of w, n0 in bits 0-3)
-// to four f16x2 registers: r[0] = (n0, n4), r[1] = (n1, n5), r[2] = (n2, n6),
-// r[3] = (n3, n7) (first of each pair in the low half). Exact: the nibble,
-// offset by 8, is placed in the mantissa of 1024 (or 16 * it in that of 1024)
-// and the offset removed with one f16x2 subtract or fma.
-__device__ __forceinline__ void int4x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
-    const uint32_t k1032 = 0x64086408u;     // (1032, 1032)
-    const uint32_t k1_16 = 0x2c002c00u;     // (1/16, 1/16)
-    const uint32_t km72 = 0xd480d480u;      // (-72, -72)
-    uint32_t w8 = w >> 8;
-    r[0] = hsub2_u32(lop3_and_xor(w, 0x000f000fu, 0x64086408u), k1032);
-    r[1] = hfma2_u32(lop3_and_xor(w, 0x00f000f0u, 0x64806480u), k1_16, km72);
-    r[2] = hsub2_u32(lop3_and_xor(w8, 0x000f000fu, 0x64086408u), k1032);
-    r[3] = hfma2_u32(lop3_and_xor(w8, 0x00f000f0u, 0x64806480u), k1_16, km72);
-}
 // Eight int4 codes (nibbles n0..n7 of w) as f16 subnormals of the offset
 // codes u = x + 8 in [1, 15]: r[0] = (u0, u4) * 2^-24, r[1] = (u1, u5) * 16 * 2^-24,
 // r[2] = (u2, u6) * 2^-24, r[3] = (u3, u7) * 16 * 2^-24. One LOP3 per register
@@ -223,9 +194,6 @@ __device__ __forceinline__ void int8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32
     uint32_t x = w ^ 0x80808080u;           // offset binary
     lo = hsub2_u32(prmt(x, 0x64646464u, 0x4140u), k1152);
     hi = hsub2_u32(prmt(x, 0x64646464u, 0x4342u), k1152);
-}
-__device__ __forceinline__ uint32_t pack_f16x2(__half lo, __half hi) {
-    return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -303,13 +271,6 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ int4 ld_dsmem_v4(uint32_t addr) {
-    int4 v;
-    asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ unsigned lanemask_lt() {

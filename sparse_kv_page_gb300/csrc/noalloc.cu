@@ -8,6 +8,8 @@
 // selection) lives in a fixed, file-scope device array instead. It runs the
 // same two kernels as locks_decode_step by calling it with that array as the
 // workspace; no existing code path changes.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "locks_internal.h"
@@ -15,29 +17,68 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(36) << 20;   // 36 MiB per GPU, held until exit
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 // Device storage; in host code this name is only a stand-in for the symbol,
 // its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's address differs per CUDA context (each context loads the module
+// anew), so the looked-up addresses are cached per (device, current context).
+struct Entry {
+    int dev;
+    CUcontext ctx;
+    void* ptr;
+};
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+Entry g_cache[kMaxContexts];
+int g_n = 0;
 
-// Device address of the scratch array on the current device (looked up once per device).
+// The driver's cuCtxGetCurrent, looked up once through the runtime.
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static const PFN_cuCtxGetCurrent_v4000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<PFN_cuCtxGetCurrent_v4000>(nullptr);
+        }
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }();
+    return fn;
+}
+
+// Device address of the scratch array in the current device's current context
+// (looked up with that device current on the first call in each context).
 int scratch_address(void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LOCKS_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return LOCKS_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return LOCKS_ERR_CUDA;
     }
-    *out = g_scratch_ptr[dev];
+    const auto get = ctx_get_current();
+    if (!get) return LOCKS_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return LOCKS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (ctx != nullptr) {
+        for (int i = 0; i < g_n; ++i)
+            if (g_cache[i].dev == dev && g_cache[i].ctx == ctx) {
+                *out = g_cache[i].ptr;
+                return LOCKS_OK;
+            }
+    }
+    // First call in this context (or no context current yet: the lookup makes the
+    // runtime's primary context of `dev` current, and it is cached under that one).
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return LOCKS_ERR_CUDA;
+    }
+    if (ctx == nullptr && (get(&ctx) != CUDA_SUCCESS || ctx == nullptr)) return LOCKS_ERR_CUDA;
+    if (g_n < kMaxContexts) g_cache[g_n++] = {dev, ctx, p};
+    *out = p;
     return LOCKS_OK;
 }
 

@@ -84,3 +84,20 @@ def test_host_validation_codes(lib):
     assert so.locks_score_pages(ctypes.byref(empty), None, S, None, None, None, None, None, 0, None) == L.LOCKS_OK
     assert so.locks_build_summaries(ctypes.byref(ok), None, None, 0, S, None, 0, None) == L.LOCKS_OK
     assert so.locks_build_summaries(ctypes.byref(ok), None, None, -1, S, None, 0, None) == L.LOCKS_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_oversized_problems_on_the_host(lib):
+    """The workspace-free decode step refuses, before any CUDA call, a problem whose
+    scratch exceeds its fixed 36 MiB array (batch 4 x 32 heads x 1M tokens needs 40 MiB)."""
+    so = lib.load_library()
+    fn = so.locks_decode_step_noalloc
+    P = ctypes.c_void_p
+    fn.argtypes = [ctypes.POINTER(lib.locks_dims_t), P, P, P, lib.locks_summaries_t, P, P, ctypes.c_int32, P, P, P]
+    fn.restype = ctypes.c_int
+    S = lib.locks_summaries_t(None, None, None, None)
+    for dims, budget in ((lib.make_dims(4, 32, 2, 65536, 4 * 65536), 512),
+                         (lib.make_dims(4, 32, 8, 65536, 4 * 65536), 2048)):
+        assert lib.locks_workspace_size(dims, budget) > (36 << 20)
+        assert fn(ctypes.byref(dims), None, None, None, S, None, None, budget, None, None, None) == \
+            lib.LOCKS_ERR_WORKSPACE_TOO_SMALL
+    assert lib.locks_workspace_size(lib.make_dims(3, 32, 8, 65536, 3 * 65536), 2048) <= (36 << 20)

@@ -20,3 +20,4 @@ def test_cpu_baseline_record_has_all_cores_and_single_thread_legs():
     assert rec["cores"] == threads
     assert rec["single_thread"]["cores"] == 1 and rec["single_thread"]["value"] > 0
     assert step.cores() == threads          # the thread count is restored afterwards
+    assert isinstance(rec["cpu_model"], str) and rec["cpu_model"]

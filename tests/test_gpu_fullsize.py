@@ -112,6 +112,24 @@ def test_full_size_decode_step(wname, budget):
     assert np.abs(got - ref_o)[heads].max() < ATT_ABS
     assert cosine(got, ref_o)[heads].min() >= ATT_COS
     assert np.abs(lse.cpu().numpy() - ref_l)[heads].max() < 1e-3
+    # every segment, including those whose selection differs at the boundary: the attention
+    # call on the step's own selection gives the step's output (up to the merge order: one
+    # bf16 step), and on the oracle's selection the oracle's output
+    for chosen, n_chosen, check in ((sel_np, nsel_np, "self"), (osel, on, "oracle")):
+        padded = np.zeros((B, Hkv, k_cap), np.int32)
+        padded[:, :, :min(k_cap, chosen.shape[2])] = chosen[:, :, :k_cap]
+        o2 = torch.zeros((B, Hq, 128), dtype=torch.int16, device=DEV)
+        l2 = torch.zeros((B, Hq), dtype=torch.float32, device=DEV)
+        L.locks_sparse_attention(dims, qd, kc, vc, td, t(padded), t(np.asarray(n_chosen, np.int32)), k_cap, o2, l2)
+        torch.cuda.synchronize()
+        g2, l2n = bf16_out(o2), l2.cpu().numpy()
+        if check == "self":
+            assert np.all(np.abs(g2 - got) <= 2.0 ** -7 * np.maximum(np.abs(g2), np.abs(got)) + 1e-6)
+            assert np.abs(l2n - lse.cpu().numpy()).max() < 1e-5
+        else:
+            assert np.abs(g2 - ref_o).max() < ATT_ABS
+            assert cosine(g2, ref_o).min() >= ATT_COS
+            assert np.abs(l2n - ref_l).max() < 1e-3
 
 
 def test_full_size_dense_attention_split_over_clusters():

@@ -311,7 +311,23 @@ def _run_decode(w, inp, mu, basis, coef, scales, budget):
     torch.cuda.synchronize()
     assert L.locks_get_device_status(ws) == 0
     return dict(out=bf16_out(out), lse=lse.cpu().numpy(), scores=scores.cpu().numpy().astype(np.float64),
-                selected=sel.cpu().numpy(), n_selected=nsel.cpu().numpy())
+                selected=sel.cpu().numpy(), n_selected=nsel.cpu().numpy(), prob=prob, k_cap=k_cap)
+
+
+def _attend_on(prob, k_cap, selected, n_selected):
+    """locks_sparse_attention on a given selection (no workspace: one cluster per segment)."""
+    B, Hq = prob.q.shape[0], prob.q.shape[1]
+    src = np.asarray(selected, np.int32)
+    padded = np.zeros(src.shape[:2] + (k_cap,), np.int32)
+    padded[:, :, :min(k_cap, src.shape[2])] = src[:, :, :k_cap]
+    sel = t(padded)
+    nsel = t(np.asarray(n_selected, np.int32))
+    out = torch.zeros((B, Hq, 128), dtype=torch.int16, device=DEV)
+    lse = torch.zeros((B, Hq), device=DEV)
+    L.locks_sparse_attention(prob.dims, prob.q, prob.k_cache, prob.v_cache, prob.page_table, sel, nsel, k_cap,
+                             out, lse)
+    torch.cuda.synchronize()
+    return bf16_out(out), lse.cpu().numpy()
 
 
 @pytest.mark.parametrize("wname,pages,batch,budget", [("tiny", None, None, 256), ("llama8b_128k", 700, 1, 2048),
@@ -339,6 +355,17 @@ def test_decode_step_matches_oracle(wname, pages, batch, budget):
     assert np.abs(got["out"] - ref["out"])[heads].max() < ATT_ABS
     assert cosine(got["out"], ref["out"])[heads].min() >= ATT_COS
     assert np.abs(got["lse"] - ref["lse"])[heads].max() < 1e-3
+    # every segment, including those whose selection differs at the boundary: the fused
+    # output is the attention over the fused step's own selection (the attention call on
+    # it, up to the merge order: one bf16 step), and the attention call on the oracle's
+    # selection reproduces the oracle's output
+    sep_out, sep_lse = _attend_on(got["prob"], got["k_cap"], got["selected"], got["n_selected"])
+    assert np.all(np.abs(sep_out - got["out"]) <= 2.0 ** -7 * np.maximum(np.abs(sep_out), np.abs(got["out"])) + 1e-6)
+    assert np.abs(sep_lse - got["lse"]).max() < 1e-5
+    orc_out, orc_lse = _attend_on(got["prob"], got["k_cap"], ref["selected"], ref["n_selected"])
+    assert np.abs(orc_out - ref["out"]).max() < ATT_ABS
+    assert cosine(orc_out, ref["out"]).min() >= ATT_COS
+    assert np.abs(orc_lse - ref["lse"]).max() < 1e-3
     # carriers (planted pages aligned with the group query) are kept
     for b in range(w.batch):
         for h in range(w.num_kv_heads):

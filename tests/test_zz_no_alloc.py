@@ -2,11 +2,13 @@
 
 Engines that keep all of HBM for their own KV pool, or that cannot afford the
 device synchronisation cudaMalloc may cause inside a decode loop, call
-locks_decode_step_noalloc, whose scratch is a fixed array inside the library.
-This file is collected last on purpose: if it fails, a run that stops at the
-first failure has already run every other test. It calls the entry point
-through the C ABI and checks that two calls in a row each reproduce the
-regular locks_decode_step output (same tolerance as the other attention tests).
+locks_decode_step_noalloc, whose scratch is a fixed 36 MiB array inside the
+library. This file is collected last on purpose: if it fails, a run that stops
+at the first failure has already run every other test. It calls the entry
+point through the C ABI and checks that two calls in a row each reproduce the
+regular locks_decode_step output exactly (both run the same two kernels on the
+same inputs), at an ordinary size and at the largest table that still fits the
+array, and that one size step beyond it is rejected.
 """
 
 import ctypes
@@ -20,7 +22,7 @@ from sparse_kv_page_gb300 import locks as L
 
 pytestmark = pytest.mark.gpu
 
-ATT_ABS = 2e-2
+SCRATCH_BYTES = 36 << 20
 
 
 def _noalloc_fn():
@@ -34,20 +36,40 @@ def _noalloc_fn():
     return fn
 
 
-def test_noalloc_decode_step_matches_decode_step_twice():
-    fn = _noalloc_fn()
+def _largest_fitting_pages(hq, hkv, budget):
+    """The largest max_pages_per_seq (batch 1) whose workspace fits the array, and the
+    next size up (which does not)."""
+    def need(m):
+        return L.locks_workspace_size(L.make_dims(1, hq, hkv, m, 1), budget)
+    lo, hi = 1, 1 << 22
+    assert need(lo) <= SCRATCH_BYTES < need(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if need(mid) <= SCRATCH_BYTES:
+            lo = mid
+        else:
+            hi = mid
+    return lo, hi
+
+
+def _run_pair(fn, pages_alloc, max_pages):
+    """Builds a seeded problem of `pages_alloc` summarised pages per sequence inside a page
+    table of width `max_pages`; returns (reference out, lse) from locks_decode_step and the
+    two no-alloc calls' (out, lse)."""
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS["llama8b_128k"].scaled(pages=700)
+    w = synth.WORKLOADS["llama8b_128k"].scaled(pages=pages_alloc)
     inp = synth.make_decode_inputs(w)
 
     def up(a):
         a = np.ascontiguousarray(a)
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
 
+    table_np = np.zeros((w.batch, max_pages), np.int32)
+    table_np[:, :w.pages] = inp.page_table
     q, kc, vc = up(inp.q), up(inp.k_cache), up(inp.v_cache)
-    table, seq = up(inp.page_table), up(inp.seq_pages)
-    dims = L.make_dims(w.batch, w.num_q_heads, w.num_kv_heads, w.pages, w.num_phys_pages)
+    table, seq = up(table_np), up(inp.seq_pages)
+    dims = L.make_dims(w.batch, w.num_q_heads, w.num_kv_heads, max_pages, w.num_phys_pages)
     summ = L.Summaries.empty(w.num_phys_pages, w.num_kv_heads, dev)
     ids = torch.arange(w.num_phys_pages, dtype=torch.int32, device=dev)
     L.locks_build_summaries(dims, kc, ids, w.num_phys_pages, summ)
@@ -58,24 +80,54 @@ def test_noalloc_decode_step_matches_decode_step_twice():
     ref_lse = torch.zeros((w.batch, w.num_q_heads), device=dev)
     L.locks_decode_step(dims, q, kc, vc, summ, table, seq, budget, ref_out, ws, lse=ref_lse)
     torch.cuda.synchronize()
-    ref = synth.bf16_bits_to_f32(ref_out.cpu().numpy().view(np.uint16))
+    assert L.locks_get_device_status(ws) == L.LOCKS_OK
 
     stream = torch.cuda.current_stream().cuda_stream
+    got = []
     for _ in range(2):
         out = torch.full((w.batch, w.num_q_heads, 128), -1, dtype=torch.int16, device=dev)
         lse = torch.full((w.batch, w.num_q_heads), float("nan"), device=dev)
         rc = fn(ctypes.byref(dims), q.data_ptr(), kc.data_ptr(), vc.data_ptr(), summ.c(), table.data_ptr(),
                 seq.data_ptr(), budget, out.data_ptr(), lse.data_ptr(), stream)
-        assert rc == 0, L.locks_status_string(rc)
+        assert rc == L.LOCKS_OK, L.locks_status_string(rc)
         torch.cuda.synchronize()
-        got = synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16))
-        assert np.abs(got - ref).max() < ATT_ABS
-        assert np.abs(lse.cpu().numpy() - ref_lse.cpu().numpy()).max() < 1e-3
+        got.append((out.cpu().numpy(), lse.cpu().numpy()))
+    return (ref_out.cpu().numpy(), ref_lse.cpu().numpy()), got
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+def test_noalloc_decode_step_equals_decode_step_twice():
     fn = _noalloc_fn()
-    dims = L.make_dims(16, 32, 8, 65536, 16 * 65536)   # 16 x 32 x 65536 fp32 scores = 128 MiB > 36 MiB
+    (ref_out, ref_lse), got = _run_pair(fn, 700, 700)
+    for out, lse in got:
+        assert np.array_equal(out, ref_out)
+        assert np.array_equal(lse, ref_lse)
+
+
+def test_noalloc_at_the_largest_fitting_table():
+    """A page table just inside the array (its score table and partials fill ~36 MiB;
+    300 pages summarised) runs and equals locks_decode_step; one size step more is
+    rejected before anything is launched."""
+    fn = _noalloc_fn()
+    fit, over = _largest_fitting_pages(32, 8, 2048)
+    need_fit = L.locks_workspace_size(L.make_dims(1, 32, 8, fit, 1), 2048)
+    assert SCRATCH_BYTES - 512 <= need_fit <= SCRATCH_BYTES
+    (ref_out, ref_lse), got = _run_pair(fn, 300, fit)
+    for out, lse in got:
+        assert np.array_equal(out, ref_out)
+        assert np.array_equal(lse, ref_lse)
+    dims = L.make_dims(1, 32, 8, over, 300)
     rc = fn(ctypes.byref(dims), None, None, None, L.locks_summaries_t(None, None, None, None), None, None, 2048,
             None, None, None)
     assert rc == L.LOCKS_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_rejects_the_4x1m_workload():
+    """Batch 4 at 32 query heads x 65536 pages needs 40 MiB of scratch: rejected."""
+    fn = _noalloc_fn()
+    dims = L.make_dims(4, 32, 2, 65536, 4 * 65536)
+    assert L.locks_workspace_size(dims, 512) > SCRATCH_BYTES
+    rc = fn(ctypes.byref(dims), None, None, None, L.locks_summaries_t(None, None, None, None), None, None, 512,
+            None, None, None)
+    assert rc == L.LOCKS_ERR_WORKSPACE_TOO_SMALL
+    dims = L.make_dims(3, 32, 8, 65536, 3 * 65536)
+    assert L.locks_workspace_size(dims, 2048) <= SCRATCH_BYTES
