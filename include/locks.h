@@ -48,9 +48,11 @@
  *   seq_pages         int32 [batch]: full (summarised) pages of each sequence,
  *                     0 <= seq_pages[b] <= max_pages_per_seq
  *   scores            fp32 [batch][num_q_heads][max_pages_per_seq]
- *   lse_partials      fp32 pairs [batch][num_q_heads][ceil(max_pages_per_seq/8)][2]:
- *                     (max, sum exp(score - max)) over each 8-page block of a
- *                     sequence (pages < seq_pages only); optional
+ *   lse_partials      fp32 pairs, locks_lse_partials_size bytes: (max, sum exp(score -
+ *                     max)) of each sequence's scores per query head, split by the
+ *                     scoring launch's CTAs and warps (an internal layout, written by
+ *                     locks_score_pages and read by the selection calls for the same
+ *                     dims on the same device); optional
  *   selected          int32 [batch][num_kv_heads][k_cap], ascending logical
  *                     page ids, k_cap = locks_k_cap(dims, budget_tokens)
  *   n_selected        int32 [batch][num_kv_heads]
@@ -150,6 +152,15 @@ LOCKS_API int locks_k_cap(const locks_dims_t* dims, int32_t budget_tokens, int32
 LOCKS_API int locks_workspace_size(const locks_dims_t* dims, int32_t budget_tokens, size_t* bytes);
 
 /*
+ * Bytes of the lse_partials buffer of locks_score_pages / locks_select_pages /
+ * locks_select_attend for these dims (16-byte aligned): one (max, sum exp) pair per
+ * (sequence, query head, scoring CTA, consumer warp), the scoring grid being at most 256
+ * CTAs. The selection reduces the per-head normaliser from them without reading the score
+ * table or exchanging partial sums between its CTAs.
+ */
+LOCKS_API int locks_lse_partials_size(const locks_dims_t* dims, size_t* bytes);
+
+/*
  * Summary build ([post] "How LOCKS works": a one-time decomposition of the
  * centred keys when a page fills, off the decode critical path; [summary] 2.1:
  * a small eigendecomposition of the centred keys, int8 centroid, int4 basis,
@@ -174,9 +185,9 @@ LOCKS_API int locks_build_summaries(const locks_dims_t* dims, const uint16_t* k_
  * for every sequence b, query head h and logical page j < seq_pages[b], with
  * the summary of unit (page_table[b][j], h / g) dequantised. Entries
  * j >= seq_pages[b] are not written. When lse_partials is not NULL it also
- * receives each 8-page block's (max, sum exp) of the scores (layout above),
- * which the selection uses to form the per-head normaliser without
- * re-reading the whole score table.
+ * receives the (max, sum exp) of the scores per query head split by the scoring
+ * CTA and warp (locks_lse_partials_size bytes), from which the selection forms the
+ * per-head normaliser without re-reading the whole score table.
  */
 LOCKS_API int locks_score_pages(const locks_dims_t* dims, const float* q, locks_summaries_t summaries,
                                 const int32_t* page_table, const int32_t* seq_pages, float* scores,
@@ -193,8 +204,9 @@ LOCKS_API int locks_score_pages(const locks_dims_t* dims, const float* q, locks_
  * lower page id, NaN keys ranked below -inf, written in ascending order;
  * n_selected[b][kvh] = k. sel_keys (fp32 [B][Hkv][max_pages_per_seq], may be
  * NULL) receives key_j for j < seq_pages[b]. lse_partials (may be NULL) are
- * the partials locks_score_pages wrote for these same scores; when given,
- * L_h is reduced from them.
+ * the partials locks_score_pages wrote for these same scores and dims on this
+ * device; when given, L_h is reduced from them. A NaN score carries no mass (it is
+ * read as -inf), so a page whose group scores are all NaN ranks last.
  */
 LOCKS_API int locks_select_pages(const locks_dims_t* dims, const float* scores, const float* lse_partials,
                                  const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected,
@@ -296,10 +308,11 @@ LOCKS_API int locks_decode_step_tail(const locks_dims_t* dims, const float* q, c
  * exits. The caller still passes all inputs and outputs (out, and lse which
  * may be NULL).
  * - Returns LOCKS_ERR_WORKSPACE_TOO_SMALL when locks_workspace_size(dims,
- *   budget_tokens) exceeds 36 MiB. The score table (4 bytes) and its LSE
- *   partials (1 byte) per (sequence, query head, page) dominate: at 32 query
- *   heads and 65536 pages (1M tokens) each sequence needs 10 MiB, so batch 3
- *   fits (30 MiB) and batch 4 (40 MiB) is rejected.
+ *   budget_tokens) exceeds 36 MiB. The score table (4 bytes per sequence,
+ *   query head and page) dominates: at 32 query heads and 65536 pages (1M
+ *   tokens) each sequence needs 8 MiB of it plus 0.1-0.3 MiB of LSE partials,
+ *   so batch 4 fits (32.5 MiB; 33 MiB with 2 kv heads) and batch 5 (40.6 MiB)
+ *   is rejected.
  * - The first call in each CUDA context (per device) looks up the array's
  *   device address with that device current and caches it for that context;
  *   make that first call before any stream capture. Resetting the device

@@ -106,6 +106,21 @@ int validate_dims(const locks_dims_t* d) {
     return LOCKS_OK;
 }
 
+// Bytes of the scorer's LSE partials: one (max, sum exp) pair per (sequence, query head,
+// scorer CTA, consumer-warp slot), for the largest scorer grid.
+size_t partials_bytes(const locks_dims_t* d) {
+    const int g = d->num_q_heads / d->num_kv_heads;
+    return static_cast<size_t>(d->batch) * d->num_q_heads * locks::kMaxScorerCtas *
+           locks::slot_warps(d->num_kv_heads, g) * 8;
+}
+
+// Grid of the scorer launch for these dims on a device with `sms` SMs available to it.
+int scorer_grid(const locks_dims_t* d, int sms) {
+    const int np = locks::kStageUnits / d->num_kv_heads;
+    const int nchunks = (d->max_pages_per_seq + np - 1) / np;
+    return locks::score_grid(d->batch * nchunks, sms);
+}
+
 int k_cap_of(const locks_dims_t* d, int32_t budget) {
     int k = budget / LOCKS_PAGE_SIZE;
     if (k > d->max_pages_per_seq) k = d->max_pages_per_seq;
@@ -121,7 +136,7 @@ WsLayout ws_layout(const locks_dims_t* d, int32_t budget) {
     w.status = 0;
     w.scores = kAlign;
     w.partials = w.scores + align_up(B * d->num_q_heads * static_cast<size_t>(d->max_pages_per_seq) * 4);
-    w.selected = w.partials + align_up(B * d->num_q_heads * static_cast<size_t>((d->max_pages_per_seq + 7) / 8) * 8);
+    w.selected = w.partials + align_up(partials_bytes(d));
     w.n_selected = w.selected + align_up(B * d->num_kv_heads * static_cast<size_t>(k_cap_of(d, budget)) * 4);
     w.total = w.n_selected + align_up(B * d->num_kv_heads * 4);
     // split attention (attention-only calls, never alongside the regions above)
@@ -222,12 +237,13 @@ int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t*
                        const int32_t* page_table, const float* scores, const float* partials,
                        const int32_t* seq_pages, const int32_t* tail_tokens,
                        int32_t budget_tokens, int32_t* selected, int32_t* n_selected, uint16_t* out, float* lse,
-                       void* workspace, cudaStream_t st) {
+                       void* workspace, cudaStream_t st, int reserve_sms = 0) {
     const int dev = current_device();
     if (dev < 0) return LOCKS_ERR_CUDA;
     locks::SelectAttendArgs a = sa_args(dims, workspace);
     a.scores = scores;
     a.lse_partials = partials;
+    a.score_grid = scorer_grid(dims, std::max(1, num_sms(dev) - reserve_sms));
     a.seq_pages = seq_pages;
     a.selected = selected;
     a.n_selected = n_selected;
@@ -278,6 +294,14 @@ int locks_workspace_size(const locks_dims_t* dims, int32_t budget_tokens, size_t
     return LOCKS_OK;
 }
 
+int locks_lse_partials_size(const locks_dims_t* dims, size_t* bytes) {
+    if (!bytes) return LOCKS_ERR_INVALID_ARG;
+    const int v = validate_dims(dims);
+    if (v != LOCKS_OK) return v;
+    *bytes = partials_bytes(dims);
+    return LOCKS_OK;
+}
+
 int locks_set_wait_limit_ns(uint64_t ns) {
     g_wait_limit_ns.store(ns == 0 ? kDefaultWaitNs : ns);
     return LOCKS_OK;
@@ -316,7 +340,7 @@ int locks_score_pages(const locks_dims_t* dims, const float* q, locks_summaries_
     if (v != LOCKS_OK) return v;
     if (dims->batch == 0 || dims->max_pages_per_seq == 0) return LOCKS_OK;
     if (!q || !page_table || !seq_pages || !scores || !aligned(q, 16)) return LOCKS_ERR_INVALID_ARG;
-    if (lse_partials && !aligned(lse_partials, 8)) return LOCKS_ERR_INVALID_ARG;
+    if (lse_partials && !aligned(lse_partials, 16)) return LOCKS_ERR_INVALID_ARG;
     if ((v = check_summaries(summaries)) != LOCKS_OK) return v;
     if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
     return score_impl(dims, q, summaries, page_table, seq_pages, scores, lse_partials, workspace,
@@ -331,6 +355,7 @@ int locks_select_pages(const locks_dims_t* dims, const float* scores, const floa
     if (budget_tokens < 0) return LOCKS_ERR_INVALID_ARG;
     if (dims->batch == 0) return LOCKS_OK;
     if (!scores || !seq_pages || !selected || !n_selected) return LOCKS_ERR_INVALID_ARG;
+    if (lse_partials && !aligned(lse_partials, 16)) return LOCKS_ERR_INVALID_ARG;
     if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
     if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelect)) return LOCKS_ERR_UNSUPPORTED;
     const int dev = current_device();
@@ -338,6 +363,7 @@ int locks_select_pages(const locks_dims_t* dims, const float* scores, const floa
     locks::SelectAttendArgs a = sa_args(dims, workspace);
     a.scores = scores;
     a.lse_partials = lse_partials;
+    a.score_grid = scorer_grid(dims, num_sms(dev));
     a.seq_pages = seq_pages;
     a.selected = selected;
     a.n_selected = n_selected;
@@ -408,6 +434,7 @@ int locks_select_attend_tail(const locks_dims_t* dims, const float* q, const uin
     if (!q || !k_cache || !v_cache || !page_table || !scores || !seq_pages || !selected || !n_selected || !out)
         return LOCKS_ERR_INVALID_ARG;
     if (!aligned(q, 8) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return LOCKS_ERR_INVALID_ARG;
+    if (lse_partials && !aligned(lse_partials, 16)) return LOCKS_ERR_INVALID_ARG;
     if (workspace && (v = check_ws(workspace, workspace_bytes, kAlign)) != LOCKS_OK) return v;
     if (!select_fits(dims->max_pages_per_seq, locks::SAMode::kSelectAttend)) return LOCKS_ERR_UNSUPPORTED;
     return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, lse_partials, seq_pages, tail_tokens,
@@ -453,7 +480,7 @@ int locks_decode_step_tail(const locks_dims_t* dims, const float* q, const uint1
         if (v != LOCKS_OK) return v;
     }
     return select_attend_impl(dims, q, k_cache, v_cache, page_table, scores, partials, seq_pages, tail_tokens,
-                              budget_tokens, selected, n_selected, out, lse, workspace, st);
+                              budget_tokens, selected, n_selected, out, lse, workspace, st, tail_tokens ? 1 : 0);
 }
 
 int locks_get_device_status(const void* workspace, int32_t* status, void* stream) {

@@ -34,6 +34,22 @@ cudaError_t ensure_kernel_attrs(int smem_bytes, bool nonportable_cluster = false
     return cudaSuccess;
 }
 
+// The scorer's persistent grid: one CTA per SM, at most kMaxScorerCtas (which bounds the
+// size of its LSE partials). CTA c scores items [c * per, (c + 1) * per) of the
+// batch * nchunks items, per = ceil(items / grid); an item is kStageUnits / Hkv
+// consecutive logical pages of one sequence (all kv heads).
+constexpr int kMaxScorerCtas = 256;
+constexpr int kStageUnits = 64;
+inline int score_grid(int total_items, int num_sms) {
+    const int g = num_sms < kMaxScorerCtas ? num_sms : kMaxScorerCtas;
+    return total_items < g ? total_items : g;
+}
+// LSE partial slots per (sequence, query head) in each scorer CTA: one per consumer warp
+// that scores that head (two groups of 8 warps take alternate stages for GQA groups of up
+// to 8 heads; for larger groups each group takes 8 of the heads; a group's 8 warps split
+// a stage's pages over 8 / Hkv blocks).
+__host__ __device__ constexpr int slot_warps(int hkv, int g) { return (g > 8 ? 1 : 2) * (8 / hkv); }
+
 struct ScoreArgs {
     const float* q;
     const int8_t* mu;
@@ -43,7 +59,9 @@ struct ScoreArgs {
     const int32_t* page_table;
     const int32_t* seq_pages;
     float* scores;
-    float* lse_partials;      // nullable: (max, sum exp) per (b, q head, 8-page block)
+    float* lse_partials;      // nullable: (max, sum exp) pairs [B][Hq][grid * slot_warps]: per
+                              // (sequence, query head, scorer CTA, consumer warp), over the
+                              // units that warp scored (-inf, 0 when none)
     int batch, hq, hkv, max_pages, num_phys;
     DeviceStatus st;
 };
@@ -52,7 +70,8 @@ cudaError_t launch_score(const ScoreArgs& a, int num_sms, cudaStream_t stream);
 struct SelectAttendArgs {
     // selection
     const float* scores;
-    const float* lse_partials;   // nullable
+    const float* lse_partials;   // nullable: the scorer's partials (ScoreArgs::lse_partials)
+    int score_grid;           // the grid of the scorer launch that wrote them
     const int32_t* seq_pages;
     int32_t* selected;        // [B][Hkv][k_cap]
     int32_t* n_selected;      // [B][Hkv]

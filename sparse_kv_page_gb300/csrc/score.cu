@@ -33,7 +33,6 @@ namespace locks {
 namespace {
 
 constexpr int kGroupWarps = 8;          // consumer warps per stage
-constexpr int kStageUnits = 64;
 constexpr int kStages = 4;
 constexpr int kStMu = 0;
 constexpr int kStBasis = kStMu + kStageUnits * 128;
@@ -58,6 +57,9 @@ struct Shape {
     static constexpr int kConsumerWarps = kGroups * kGroupWarps;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
 };
+
+template <int HKV, int HS>
+constexpr int kSlotWarps = slot_warps(HKV, HS == 2 ? 16 : 8);
 
 template <int HKV, int NT, int HS>
 __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs a, int nchunks, int total_items) {
@@ -179,10 +181,35 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
         float qsum[NT];    // sum of that head's pre-scaled query q' (code-offset correction)
         float qsc[NT];     // 2^e of the output head (4 nt + t) of this thread
         int cur_b = -1, q_b = -1, cur_P = 0;
+        // this warp's (max, sum exp) of the scores of its heads over the units it scored of
+        // sequence cur_b (lanes 0-3: head hoff + 4 nt + t), written to its slot when the
+        // sequence changes and at the end (every sequence of this CTA's range gets a slot)
+        float run_m[NT], run_l[NT];
+        const int wslot = (HS == 1 ? group * (kGroupWarps / HKV) : 0) + blk;
+        const int nslots = gridDim.x * kSlotWarps<HKV, HS>;
+        auto flush_partials = [&](int pb) {
+            if (a.lse_partials && pb >= 0 && gid == 0) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int hh = hoff + 4 * nt + t;
+                    if (hh < g)
+                        reinterpret_cast<float2*>(a.lse_partials)
+                            [(static_cast<int64_t>(pb) * a.hq + kvh * g + hh) * nslots +
+                             blockIdx.x * kSlotWarps<HKV, HS> + wslot] = make_float2(run_m[nt], run_l[nt]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                run_m[nt] = -INFINITY;
+                run_l[nt] = 0.f;
+            }
+        };
+        flush_partials(-1);
         uint32_t k = 0;
         for (int it = it0; it < it1; ++it) {
             const int b = it / nchunks, page0 = (it % nchunks) * NP;
             if (b != cur_b) {
+                flush_partials(cur_b);
                 cur_b = b;
                 cur_P = min(a.seq_pages[b], a.max_pages);
             }
@@ -395,9 +422,8 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                     score_out[nt] = a_raw * smu_row * qsc[nt] * kInvSqrtD + lse[nt];
                 }
                 if (a.lse_partials) {
-                    // (max, sum exp) of this warp's 8 pages for each head: one partial per 8-page block
-                    const int nblk = (a.max_pages + 7) / 8;
-                    const int blk8 = (page0 + 8 * blk) / 8;
+                    // (max, sum exp) of this warp's 8 pages for each head, folded into the
+                    // warp's running partial of the sequence
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const float sv = gid < nv ? score_out[nt] : -INFINITY;
@@ -405,14 +431,15 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
                         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                        float z = (sv == -INFINITY) ? 0.f : fast_exp2((sv - m) * kLog2e);
+                        float z = (sv == -INFINITY || sv != sv) ? 0.f : fast_exp2((sv - m) * kLog2e);
                         z += __shfl_xor_sync(0xffffffffu, z, 4);
                         z += __shfl_xor_sync(0xffffffffu, z, 8);
                         z += __shfl_xor_sync(0xffffffffu, z, 16);
-                        const int hh = hoff + 4 * nt + t;
-                        if (gid == 0 && hh < g)
-                            reinterpret_cast<float2*>(a.lse_partials)
-                                [(static_cast<int64_t>(b) * a.hq + kvh * g + hh) * nblk + blk8] = make_float2(m, z);
+                        if (z > 0.f) {
+                            const float M = fmaxf(run_m[nt], m);
+                            run_l[nt] = run_l[nt] * fast_exp2((run_m[nt] - M) * kLog2e) + z * fast_exp2((m - M) * kLog2e);
+                            run_m[nt] = M;
+                        }
                     }
                 }
                 if (gid < nv) {
@@ -430,6 +457,7 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
             if (lane == 0) mbar_arrive(&empty[s]);
             ++k;
         }
+        flush_partials(cur_b);
     }
     if (failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
 }
@@ -443,7 +471,7 @@ cudaError_t launch_t(const ScoreArgs& a, int num_sms, cudaStream_t stream) {
     cudaError_t e = ensure_kernel_attrs<score_kernel<HKV, NT, HS>>(kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(min(total, num_sms), 1, 1);
+    cfg.gridDim = dim3(score_grid(total, num_sms), 1, 1);
     cfg.blockDim = dim3(Shape<NT>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

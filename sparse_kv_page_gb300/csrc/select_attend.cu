@@ -51,6 +51,15 @@ constexpr int kRingBytes = ((kWarps * kPageSlotBytes > kWarpPartBytes ? kWarps *
 constexpr int kMaxG = LOCKS_MAX_GROUP;
 constexpr int kQRow = 136;                            // bf16 per staged query row (128 + 8 pad)
 constexpr int kRankCap = 256;                         // radix early exit: largest bin ranked directly
+constexpr int kCandCap = 768;                         // fast selection: candidates gathered per segment
+constexpr int kCandListBytes = kCandCap * 12;         // a list of (key, logical page, physical page)
+constexpr int kStageBytes = 64 * 1024;                // staged score rows (four heads) of a CTA's pages
+static_assert(kStageBytes <= kRingBytes, "the staged scores share the attention ring's space");
+// Shared memory after SmallShared: region A (the keys, which overlay the staged score rows,
+// then the attention ring), then (selection) the published and the gathered candidate lists.
+__host__ __device__ constexpr int region_a_bytes(int chunk) {
+    return ((chunk * 4 + 1023) / 1024 * 1024) > kRingBytes ? (chunk * 4 + 1023) / 1024 * 1024 : kRingBytes;
+}
 
 struct SmallShared {
     uint16_t qs[2][16 * kQRow];           // query rows (group heads), bf16 high / low parts
@@ -67,9 +76,16 @@ struct SmallShared {
     uint32_t bin_keys[256], rank_keys[256];
     uint8_t rank_src[256];
     uint64_t bar[kWarps];
+    uint64_t sbar;                        // staged score rows (selection)
+    int pub_n;                            // fast selection: this CTA's published candidates
+    int cnt_r[16];                        // ... and every CTA's count
     float cpart[kMaxG * kPartStride];     // this CTA's attention partial per head
     int split_last;                       // split attention: this cluster merges the splits of a head
 };
+
+// Two CTAs share an SM up to 4096 pages per CTA (the 1M-token context over 16 CTAs).
+static_assert(sizeof(SmallShared) + 1024 + kRingBytes + 2 * kCandListBytes <= 113 * 1024,
+              "shared memory of two select/attend CTAs per SM");
 
 // Byte offset of (token row, dim) in a page slot's K (or V) half: box = dim / 64,
 // 16-byte chunk (dim % 64) / 8 swizzled with the row.
@@ -85,12 +101,6 @@ __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float 
 }
 
 // ------------------------------------------------------------- selection
-// Per-head normaliser L_h over the sequence (cluster-wide) and the group keys of
-// this CTA's pages [j0, j1) into keys[] (order-preserving uint32 images).
-// Scores are read in batches of kB pages per thread, each batch's loads issued
-// one batch ahead (the first one before the normaliser's reduction, so its
-// latency overlaps the cluster exchange). Loops stay rolled: this code runs
-// about once per launch, and its instruction fetch is what it waits on.
 // Stores the group's query rows (scaled by log2(e)/sqrt(d)) in shared memory as bf16
 // high and low parts; the attention's MMA A fragments are read back with ldmatrix.
 __device__ __forceinline__ void store_query(const float (&qv)[16 * kD / kThreads], int g, SmallShared& sh) {
@@ -113,92 +123,217 @@ __device__ __forceinline__ void load_query(const SelectAttendArgs& a, int b, int
     }
 }
 
-// stage_q: also stage the query rows for the attention that follows (their loads
-// overlap the normaliser's).
-template <int CL, int GM>
-__device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, uint32_t* keys,
-                           SmallShared& sh, bool stage_q) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = a.hq / a.hkv;
-    const int nloc = j1 - j0;
-    const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * a.max_pages;
-    constexpr int kB = GM <= 4 ? 4 : 1;   // pages per thread per batch
-    constexpr int kStep = kB * kThreads;
-    auto load_batch = [&](float (&x)[kB][GM], int jb) {
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const int j = jb + u * kThreads;
-#pragma unroll
-            for (int hh = 0; hh < GM; ++hh)
-                x[u][hh] = (hh < g && j < j1) ? srow[static_cast<int64_t>(hh) * a.max_pages + j] : -INFINITY;
-        }
-    };
-    // the first two batches of scores are in flight during the normaliser below, and
-    // two stay in flight in the key loop
-    float v[kB][GM], v2[kB][GM];
-    load_batch(v, j0 + tid);
-    load_batch(v2, j0 + tid + kStep);
-    float qv[16 * kD / kThreads];
-    if (stage_q) load_query(a, b, kvh, g, qv);
+// Score reads: a thread takes kSL slabs of 4 consecutive pages per round (slab i of the
+// round at page jr starts at jr + 4 (tid + i kThreads)) and kHB query heads at a time.
+// A NaN score carries no mass (read as -inf), as do pages at or past j1 and heads >= g.
+constexpr int kSL = 4;
+constexpr int kRoundPages = kSL * 4 * kThreads;   // 4096
+constexpr int kHB = 4;
+struct ScoreRound {
+    float4 v[kSL][kHB];
+};
 
-    // 1. per-head log-sum-exp over the sequence's pages: (m, l) per thread and head
+__device__ __forceinline__ float no_nan(float x) { return x == x ? x : -INFINITY; }
+
+// From global memory (128-bit loads when rows are 16-byte aligned), heads [h0, h0 + kHB).
+__device__ __forceinline__ void load_round(const float* srow, int64_t stride, int g, int h0, int jr, int j1,
+                                           bool vec, ScoreRound& x) {
+#pragma unroll
+    for (int i = 0; i < kSL; ++i) {
+        const int j = jr + 4 * (static_cast<int>(threadIdx.x) + i * kThreads);
+#pragma unroll
+        for (int hh = 0; hh < kHB; ++hh) {
+            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (h0 + hh < g && j < j1) {
+                const float* p = srow + static_cast<int64_t>(h0 + hh) * stride + j;
+                if (vec) {
+                    v = __ldcg(reinterpret_cast<const float4*>(p));
+                } else {
+                    v.x = __ldcg(p);
+                    if (j + 1 < j1) v.y = __ldcg(p + 1);
+                    if (j + 2 < j1) v.z = __ldcg(p + 2);
+                    if (j + 3 < j1) v.w = __ldcg(p + 3);
+                }
+            }
+            x.v[i][hh] = v;
+        }
+    }
+}
+// From the staged rows in shared memory (row hh of the batch at stg + hh * chunk; off is
+// the round's first page relative to the CTA's first page).
+__device__ __forceinline__ void load_round_smem(const float* stg, int chunk, int nh, int off, int nloc,
+                                                ScoreRound& x) {
+#pragma unroll
+    for (int i = 0; i < kSL; ++i) {
+        const int jj = off + 4 * (static_cast<int>(threadIdx.x) + i * kThreads);
+#pragma unroll
+        for (int hh = 0; hh < kHB; ++hh) {
+            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (hh < nh && jj < nloc) v = *reinterpret_cast<const float4*>(stg + hh * chunk + jj);
+            x.v[i][hh] = v;
+        }
+    }
+}
+__device__ __forceinline__ float round_val(const ScoreRound& x, int i, int hh, int e, int j, int j1) {
+    const float4 v = x.v[i][hh];
+    const float s = e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+    return j + e < j1 ? no_nan(s) : -INFINITY;
+}
+
+__device__ __forceinline__ void lse_combine_safe(float& m, float& l, float m2, float l2) {
+    if (!(l2 > 0.f) || m2 == -INFINITY || m2 != m2) return;   // empty or corrupt partial
+    lse_combine(m, l, m2, l2);
+}
+
+// The first radix digit of the selection (fast path). Keys are log mass shares that sum
+// to 1 over the sequence (each head's shares sum to 1 and a key is the group mean), so at
+// most K - 1 keys exceed -ln K, and the K-th largest lies above -ln P (P pages; the mean
+// share is 1/P) unless K is a large fraction of P. The
+// first pass counts the keys' order-preserving uint32 images u in 256 bins of 2^s images
+// spanning [lo, hi], hi = -ln K + 1/4, lo = -ln P; keys below / above the span fall in
+// bins 0 / 255 (bin 0 -- about half of the keys -- is counted by difference, without
+// atomics). If the K-th key lands in bin 0 or 255 the selection
+// restarts as a plain MSB-first radix over the whole key (exact either way).
+struct RadixRange {
+    uint32_t base;   // u of the first image of bin 0
+    uint64_t top;    // one past the last image of bin 255 (<= 2^32)
+    uint32_t last;   // top - 1
+    int s;           // log2 of the bin width
+};
+__device__ __forceinline__ RadixRange fast_range(int K, int P) {
+    const float hi = -logf(static_cast<float>(K)) + 0.25f;
+    const float lo = -logf(static_cast<float>(P));
+    const uint32_t uhi = orderable_key(hi), ulo = orderable_key(lo);   // hi > lo since K < P
+    const uint64_t span = static_cast<uint64_t>(uhi) - ulo + 1;
+    RadixRange r;
+    r.s = 0;
+    while ((256ull << r.s) < span) ++r.s;
+    r.top = static_cast<uint64_t>(uhi) + 1;
+    if (r.top > (256ull << r.s)) {
+        r.base = static_cast<uint32_t>(r.top - (256ull << r.s));
+    } else {
+        r.base = 0u;
+        r.top = 256ull << r.s;
+    }
+    r.last = static_cast<uint32_t>(r.top - 1);
+    return r;
+}
+__device__ __forceinline__ uint32_t fast_digit(uint32_t u, const RadixRange& r) {
+    if (u < r.base) return 0u;
+    if (u > r.last) return 255u;
+    return (u - r.base) >> r.s;
+}
+
+// Per-head normaliser L_h of sequence b into sh.Lh[0..g) (the same in every CTA).
+// From the scorer's LSE partials (its launch of grid a.score_grid wrote one (max, sum exp)
+// per scorer CTA and consumer warp that scored the head): warp w reduces heads w, w + 8
+// over the partials of the scorer CTAs whose item range covers sequence b; no exchange.
+// Without partials: each CTA reduces its own pages' scores (staged rows or global
+// loads) and the CTAs exchange their (max, sum) through DSMEM.
+template <int CL, int GM>
+__device__ void normaliser(const SelectAttendArgs& a, int b, int kvh, int g, int j0, int j1, bool staged,
+                           const float* stg, int chunk, SmallShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (a.lse_partials) {
+        const int np = kStageUnits / a.hkv;
+        const int nchunks = (a.max_pages + np - 1) / np;
+        const int grid = max(1, a.score_grid);
+        const int per = max(1, (a.batch * nchunks + grid - 1) / grid);   // no items: c_hi < c_lo, n = 0
+        const int W = slot_warps(a.hkv, g);
+        const int c_lo = (b * nchunks) / per;
+        const int c_hi = min(grid - 1, ((b + 1) * nchunks - 1) / per);
+        const int n = (c_hi - c_lo + 1) * W;
+#pragma unroll 1
+        for (int hh = warp; hh < g; hh += kWarps) {
+            const float2* row = reinterpret_cast<const float2*>(a.lse_partials) +
+                                (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * grid * W + c_lo * W;
+            float m = -INFINITY, l = 0.f;
+            // two (max, sum) pairs per 16-byte load (a slot row starts on an even pair: W is even)
+#pragma unroll 1
+            for (int i0 = 0; i0 < n; i0 += 2 * 32 * 8) {
+                float4 v[8];   // all in flight before any use
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + 2 * (lane + 32 * u);
+                    v[u] = i < n ? __ldcg(reinterpret_cast<const float4*>(row + i))
+                                 : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+                }
+                // an empty or corrupt pair (sum not > 0, or a NaN) contributes nothing
+                float mm[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    mm[2 * u] = (v[u].y > 0.f && v[u].x == v[u].x) ? v[u].x : -INFINITY;
+                    mm[2 * u + 1] = (v[u].w > 0.f && v[u].z == v[u].z) ? v[u].z : -INFINITY;
+                }
+                float M = m;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) M = fmaxf(M, mm[k]);
+                if (M != -INFINITY) {
+                    float z = m == -INFINITY ? 0.f : l * fast_exp2((m - M) * kLog2e);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        z += mm[2 * u] == -INFINITY ? 0.f : v[u].y * fast_exp2((mm[2 * u] - M) * kLog2e);
+                        z += mm[2 * u + 1] == -INFINITY ? 0.f : v[u].w * fast_exp2((mm[2 * u + 1] - M) * kLog2e);
+                    }
+                    m = M;
+                    l = z;
+                }
+            }
+            float M = m;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float z = (m == -INFINITY) ? 0.f : l * fast_exp2((m - M) * kLog2e);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            if (lane == 0) sh.Lh[hh] = (z > 0.f) ? M + logf(z) : -INFINITY;
+        }
+        __syncthreads();
+        return;
+    }
+
+    // from this CTA's scores, then a cluster exchange
+    const int64_t stride = a.max_pages;
+    const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * stride;
+    const bool vec = (a.max_pages & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
+    constexpr int kBatches = (GM + kHB - 1) / kHB;
     float m[GM], l[GM];
 #pragma unroll
     for (int hh = 0; hh < GM; ++hh) {
         m[hh] = -INFINITY;
         l[hh] = 0.f;
     }
-    if (a.lse_partials) {
-        // from the scoring kernel's (max, sum) partials of 8-page blocks
-        const int nblk = (a.max_pages + 7) / 8;
-        const int blk0 = j0 / 8, blk1 = nloc > 0 ? (j1 + 7) / 8 : blk0;   // an empty range owns no block
-        const float2* prow = reinterpret_cast<const float2*>(a.lse_partials) +
-                             (static_cast<int64_t>(b) * a.hq + kvh * g) * nblk;
 #pragma unroll 1
-        for (int ib = blk0 + tid; ib < blk1; ib += kThreads) {
-            float2 pv[GM];
+    for (int jr = j0; jr < j1; jr += kRoundPages) {
 #pragma unroll
-            for (int hh = 0; hh < GM; ++hh)
-                pv[hh] = hh < g ? prow[static_cast<int64_t>(hh) * nblk + ib] : make_float2(-INFINITY, 0.f);
+        for (int bt = 0; bt < kBatches; ++bt) {
+            ScoreRound x;
+            if (staged && bt == 0)
+                load_round_smem(stg, chunk, min(g, kHB), jr - j0, j1 - j0, x);
+            else
+                load_round(srow, stride, g, bt * kHB, jr, j1, vec, x);
 #pragma unroll
-            for (int hh = 0; hh < GM; ++hh)
-                if (hh < g) lse_combine(m[hh], l[hh], pv[hh].x, pv[hh].y);
-        }
-    } else {
-        // from the scores themselves (reloading them later if they span several batches)
-#pragma unroll 1
-        for (int jb = j0 + tid; jb < j1; jb += kStep) {
-            float x[kB][GM];
-            if (jb == j0 + tid) {
+            for (int hh = 0; hh < kHB; ++hh) {
+                const int h = bt * kHB + hh;
+                if (h >= g || h >= GM) continue;
+                float bm = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < kB; ++u)
+                for (int i = 0; i < kSL; ++i) {
+                    const int j = jr + 4 * (tid + i * kThreads);
 #pragma unroll
-                    for (int hh = 0; hh < GM; ++hh) x[u][hh] = v[u][hh];
-            } else if (jb == j0 + tid + kStep) {
-#pragma unroll
-                for (int u = 0; u < kB; ++u)
-#pragma unroll
-                    for (int hh = 0; hh < GM; ++hh) x[u][hh] = v2[u][hh];
-            } else {
-                load_batch(x, jb);
-            }
-#pragma unroll
-            for (int hh = 0; hh < GM; ++hh) {
-                if (hh < g) {
-                    float bm = x[0][hh];
-#pragma unroll
-                    for (int u = 1; u < kB; ++u) bm = fmaxf(bm, x[u][hh]);
-                    if (bm != -INFINITY) {
-                        float z = 0.f;
-#pragma unroll
-                        for (int u = 0; u < kB; ++u) z += fast_exp2((x[u][hh] - bm) * kLog2e);
-                        lse_combine(m[hh], l[hh], bm, z);
-                    }
+                    for (int e = 0; e < 4; ++e) bm = fmaxf(bm, round_val(x, i, hh, e, j, j1));
                 }
+                if (bm == -INFINITY) continue;
+                float z = 0.f;
+#pragma unroll
+                for (int i = 0; i < kSL; ++i) {
+                    const int j = jr + 4 * (tid + i * kThreads);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) z += fast_exp2((round_val(x, i, hh, e, j, j1) - bm) * kLog2e);
+                }
+                lse_combine(m[h], l[h], bm, z);
             }
         }
     }
-    if (stage_q) store_query(qv, g, sh);   // read after the barriers below
     // warp reduction: max first, then the sums rescaled to it
 #pragma unroll
     for (int hh = 0; hh < GM; ++hh) {
@@ -249,55 +384,209 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
         sh.Lh[tid] = (z > 0.f) ? M + logf(z) : -INFINITY;
     }
     __syncthreads();
+}
 
-    // 2. group-mean mass-share keys
-    // (log2 domain: x = (s - L_h) log2 e; key = (max + log2 sum exp2(x - max)) ln 2 - ln g)
-    const float log_g = logf(static_cast<float>(g));
-    float Lr[GM];
+// Bulk copy of rows [h0, h0 + nh) of this CTA's score columns [j0, j0 + nloc) to the
+// staging buffer (row hh at stg + hh * chunk), completing on sh.sbar. One thread.
+__device__ __forceinline__ void stage_rows(const float* srow, int64_t stride, int h0, int nh, int j0, int nloc,
+                                           int chunk, float* stg, SmallShared& sh) {
+    const uint32_t bytes = static_cast<uint32_t>((nloc + 3) & ~3) * 4u;   // within the row: max_pages % 4 == 0
+    mbar_arrive_expect_tx(&sh.sbar, bytes * static_cast<uint32_t>(nh));
+    for (int hh = 0; hh < nh; ++hh) bulk_g2s(stg + hh * chunk, srow + (h0 + hh) * stride + j0, bytes, &sh.sbar);
+}
+
+// Loads the scores of heads [h0, h0 + kHB) of the 4-page slab at page j (relative jj to
+// the CTA's first page) from the staged rows (row hh at stg + hh * chunk) or from global
+// memory; heads >= g read as -inf. Values of pages at or past j1 are not meaningful.
+__device__ __forceinline__ void load_slab(const float* stg, int chunk, const float* srow, int64_t stride, int g,
+                                          int h0, int j, int jj, int j1, bool staged, bool vec, float4 (&v)[kHB]) {
 #pragma unroll
-    for (int hh = 0; hh < GM; ++hh) Lr[hh] = hh < g ? sh.Lh[hh] : 0.f;
-#pragma unroll 1
-    for (int jb = j0 + tid; jb < j1; jb += kStep) {
-        float w[kB][GM];
-        const bool more = jb + 2 * kStep < j1;
-        if (more) load_batch(w, jb + 2 * kStep);   // two batches in flight while this one is used
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const int j = jb + u * kThreads;
-            if (j < j1) {
-                float mx = -INFINITY;
-                float x[GM];
-#pragma unroll
-                for (int hh = 0; hh < GM; ++hh) {
-                    x[hh] = 0.f;
-                    if (hh < g) {
-                        x[hh] = (v[u][hh] - Lr[hh]) * kLog2e;
-                        mx = fmaxf(mx, x[hh]);
-                    }
-                }
-                float key;
-                if (mx == -INFINITY) {
-                    key = -INFINITY;
+    for (int hh = 0; hh < kHB; ++hh) {
+        float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (h0 + hh < g) {
+            if (staged) {
+                x = *reinterpret_cast<const float4*>(stg + hh * chunk + jj);
+            } else {
+                const float* p = srow + static_cast<int64_t>(h0 + hh) * stride + j;
+                if (vec) {
+                    x = __ldcg(reinterpret_cast<const float4*>(p));
                 } else {
-                    float z = 0.f;
-#pragma unroll
-                    for (int hh = 0; hh < GM; ++hh)
-                        if (hh < g) z += fast_exp2(x[hh] - mx);
-                    key = (mx + fast_log2(z)) * kLn2 - log_g;
+                    x.x = __ldcg(p);
+                    if (j + 1 < j1) x.y = __ldcg(p + 1);
+                    if (j + 2 < j1) x.z = __ldcg(p + 2);
+                    if (j + 3 < j1) x.w = __ldcg(p + 3);
                 }
-                keys[j - j0] = orderable_key(key);
-                if (a.sel_keys) a.sel_keys[(static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages + j] = key;
             }
         }
+        v[hh] = x;
+    }
+}
+__device__ __forceinline__ float comp(const float4& v, int e) {
+    return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+}
+
+// The group keys of this CTA's pages [j0, j1) into keys[] (order-preserving uint32 images)
+// and, when hist0, the fast first radix pass's histogram of them into sh.hist[0] (zeroed
+// by the caller), from sh.Lh. In the log2 domain x_h = s_h log2 e - L_h log2 e <= 0 and
+// key = log2(sum_h 2^x_h) ln 2 - ln g; each term is at most 1, so the sum needs no shift
+// unless it underflows (every share below 2^-100), when the page is redone with its
+// largest term factored out. A NaN score makes its page's key NaN (ranked last).
+// Staged scores (see select_pages) are read from shared memory, a batch of four heads at
+// a time (groups of more than four heads re-stage the next batch after each); keys[]
+// overlays the first staged row, each thread reading a slab's scores before writing its
+// keys. Otherwise the scores are read from global memory.
+template <int GM>
+__device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, int chunk, uint32_t* keys,
+                           SmallShared& sh, bool staged, const RadixRange& fr, bool hist0, uint32_t* whist,
+                           bool& failed) {
+    const int tid = threadIdx.x;
+    const int g = a.hq / a.hkv;
+    const int nloc = j1 - j0;
+    const int64_t stride = a.max_pages;
+    const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * stride;
+    const bool vec = (a.max_pages & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
+    const float* stg = reinterpret_cast<const float*>(keys);
+    const float log_g = logf(static_cast<float>(g));
+    float Lp[GM];
 #pragma unroll
-        for (int u = 0; u < kB; ++u)
+    for (int hh = 0; hh < GM; ++hh) Lp[hh] = hh < g ? sh.Lh[hh] * kLog2e : 0.f;
+    float* kout = a.sel_keys ? a.sel_keys + (static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages : nullptr;
+    // key of one page from its log2-domain total (m, z): the largest term 2^m, the sum
+    // z of 2^(x - m); counts it and writes the optional key output
+    auto finish = [&](int j, float key2) -> uint32_t {
+        const float key = key2 * kLn2 - log_g;
+        const uint32_t u = orderable_key(key);
+        if (j < j1) {
+            const uint32_t d = fast_digit(u, fr);
+            if (hist0 && d != 0u) atomicAdd(&whist[(threadIdx.x >> 5) * 256 + d], 1u);   // this warp's counts
+            if (kout) kout[j] = key;
+        }
+        return u;
+    };
+    if constexpr (GM <= kHB) {
+        // a rolled loop over this thread's slabs (instruction fetch is part of this code's
+        // latency: it runs about once per launch), the slab's four pages in parallel
+#pragma unroll 1
+        for (int jr = j0; jr < j1; jr += kRoundPages) {
+#pragma unroll 1
+            for (int i = 0; i < kSL; ++i) {
+                const int j = jr + 4 * (tid + i * kThreads);   // consecutive threads, consecutive slabs
+                if (j >= j1) break;
+                float4 v[kHB];
+                load_slab(stg, chunk, srow, stride, g, 0, j, j - j0, j1, staged, vec, v);
+                uint32_t k4[4];
 #pragma unroll
-            for (int hh = 0; hh < GM; ++hh) {
-                v[u][hh] = v2[u][hh];
-                if (more) v2[u][hh] = w[u][hh];
+                for (int e = 0; e < 4; ++e) {
+                    float x[kHB], z = 0.f;
+#pragma unroll
+                    for (int hh = 0; hh < kHB; ++hh) {
+                        x[hh] = hh < g ? fmaf(comp(v[hh], e), kLog2e, -Lp[hh]) : -INFINITY;
+                        z += fast_exp2(x[hh]);
+                    }
+                    float key2 = fast_log2(z);
+                    if (!(z >= 7.9e-31f) && z == z) {   // underflow (2^-100): factor out the largest term
+                        float m = x[0];
+#pragma unroll
+                        for (int hh = 1; hh < kHB; ++hh) m = fmaxf(m, x[hh]);
+                        float zz = 0.f;
+#pragma unroll
+                        for (int hh = 0; hh < kHB; ++hh) zz += fast_exp2(x[hh] - m);
+                        key2 = m == -INFINITY ? -INFINITY : m + fast_log2(zz);
+                    }
+                    k4[e] = finish(j + e, key2);
+                }
+                // keys[] has room for whole slabs (chunk is a multiple of 8)
+                *reinterpret_cast<uint4*>(keys + (j - j0)) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
             }
+        }
+    } else {
+        constexpr int kBatches = (GM + kHB - 1) / kHB;
+        const int nbt = (g + kHB - 1) / kHB;
+#pragma unroll 1
+        for (int jr = j0; jr < j1; jr += kRoundPages) {
+            float pm[kSL * 4], pz[kSL * 4];   // per page of this thread: largest term and sum (log2)
+#pragma unroll
+            for (int p = 0; p < kSL * 4; ++p) {
+                pm[p] = -INFINITY;
+                pz[p] = 0.f;
+            }
+#pragma unroll 1
+            for (int bt = 0; bt < nbt && bt < kBatches; ++bt) {
+                if (staged && bt > 0) {
+                    // the next four rows into the staging buffer once every thread has read it
+                    __syncthreads();
+                    if (tid == 0) {
+                        fence_proxy_async_smem();
+                        stage_rows(srow, stride, bt * kHB, min(g - bt * kHB, kHB), j0, nloc, chunk,
+                                   reinterpret_cast<float*>(keys), sh);
+                    }
+                }
+                if (staged && !mbar_wait_bounded(&sh.sbar, static_cast<uint32_t>(bt & 1), a.st.wait_limit_ns))
+                    failed = true;
+                float Lb[kHB];
+#pragma unroll
+                for (int hh = 0; hh < kHB; ++hh) {
+                    float L = 0.f;
+#pragma unroll
+                    for (int h = 0; h < GM; ++h) L = (h == bt * kHB + hh) ? Lp[h] : L;
+                    Lb[hh] = L;
+                }
+#pragma unroll
+                for (int i = 0; i < kSL; ++i) {
+                    const int j = jr + 4 * (tid + i * kThreads);
+                    if (j >= j1) continue;
+                    float4 v[kHB];
+                    load_slab(stg, chunk, srow, stride, g, bt * kHB, j, j - j0, j1, staged, vec, v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int p = 4 * i + e;
+                        float x[kHB], mr = -INFINITY;
+#pragma unroll
+                        for (int hh = 0; hh < kHB; ++hh) {
+                            x[hh] = bt * kHB + hh < g ? fmaf(comp(v[hh], e), kLog2e, -Lb[hh]) : -INFINITY;
+                            mr = fmaxf(mr, x[hh]);
+                        }
+                        if (mr == -INFINITY) continue;
+                        float zr = 0.f;
+#pragma unroll
+                        for (int hh = 0; hh < kHB; ++hh) zr += fast_exp2(x[hh] - mr);
+                        const float M = fmaxf(pm[p], mr);
+                        pz[p] = pz[p] * fast_exp2(pm[p] - M) + zr * fast_exp2(mr - M);
+                        pm[p] = M;
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kSL; ++i) {
+                const int j = jr + 4 * (tid + i * kThreads);
+                if (j >= j1) continue;
+                uint32_t k4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int p = 4 * i + e;
+                    k4[e] = finish(j + e, pm[p] == -INFINITY ? -INFINITY : pm[p] + fast_log2(pz[p]));
+                }
+                *reinterpret_cast<uint4*>(keys + (j - j0)) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+            }
+        }
     }
     __syncthreads();
+    if (hist0) {
+        // the warps' counts summed per bin; bin 0 (keys below the fast range) by difference
+        uint32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) c += whist[w * 256 + tid];
+        sh.hist[0][tid] = c;
+        __syncthreads();
+        if (tid < 32) {
+            uint32_t t = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t += sh.hist[0][8 * tid + k];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (tid == 0) sh.hist[0][0] = static_cast<uint32_t>(nloc) - t;
+        }
+    }
 }
 
 // Ordered compaction: visits the keys kept by (T, take_eq) -- every key > T and the
@@ -364,154 +653,228 @@ __device__ int ordered_keep(const uint32_t* keys, int n, uint32_t T, int take_eq
     return gt_all + min(eq_all, take_eq);
 }
 
-// Writes selected[b][kvh][0..K) and n_selected[b][kvh]; returns K.
-// One MSB-first radix select over the cluster (4 passes of 8 bits): each CTA
-// histograms its own keys, every CTA sums the CTAs' histograms through DSMEM and
-// picks the digit. The same pass also yields, per CTA, how many keys lie above
-// the chosen bin in lower-ranked CTAs and in this one (and, in the last pass,
-// how many equal T), which places this CTA's kept keys in the ascending output
-// without a further exchange.
-template <int CL, int GM>
-__device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk, uint32_t* keys,
-                            SmallShared& sh, bool stage_q) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int P = max(0, min(a.seq_pages[b], a.max_pages));
-    const int j0 = min(P, static_cast<int>(rank) * chunk);
-    const int j1 = min(P, j0 + chunk);
-    const int nloc = j1 - j0;
-
-    group_keys<CL, GM>(a, b, kvh, j0, j1, keys, sh, stage_q);
-
-    int K = min(a.budget_pages, min(P, a.k_cap));
-    K = max(K, 0);
-    int32_t* out = a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap;
-    if (rank == 0 && tid == 0) a.n_selected[b * a.hkv + kvh] = K;
-    if (K == 0) return 0;
-    if (K == P) {
-        for (int j = j0 + tid; j < j1; j += kThreads) out[j] = j;
-        return K;
+// Exclusive prefix sums over the block of three values per thread (thread t holds
+// elements 3t .. 3t + 2, in order); returns the total. Uses sh.wcnt.
+__device__ __forceinline__ int block_scan3(int (&v)[3], SmallShared& sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int own = v[0] + v[1] + v[2];
+    int inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
     }
+    __syncthreads();   // sh.wcnt free
+    if (lane == 31) sh.wcnt[warp][0] = inc;
+    __syncthreads();
+    int pre = inc - own, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        pre += w < warp ? sh.wcnt[w][0] : 0;
+        total += sh.wcnt[w][0];
+    }
+    const int v0 = v[0], v1 = v[1];
+    v[0] = pre;
+    v[1] = pre + v0;
+    v[2] = pre + v0 + v1;
+    return total;
+}
 
-    uint32_t prefix = 0;
-    int remaining = K;
-    int gt_low = 0, gt_own = 0, eq_low = 0, eq_own = 0;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        uint32_t* hist = sh.hist[pass & 1];   // alternating: other CTAs read the previous one
-        hist[tid] = 0u;
-        __syncthreads();
-        if (pass == 0) {
-            // the top byte takes few values: one shared atomic per distinct bin per warp step
-            for (int i0 = 0; i0 < nloc; i0 += kThreads) {
-                const int i = i0 + tid;
-                const uint32_t bin = i < nloc ? keys[i] >> 24 : 0xffffffffu;
-                const unsigned peers = __match_any_sync(0xffffffffu, bin);
-                if (i < nloc && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
-            }
-        } else {
-            const uint32_t hp = prefix >> (shift + 8);
-#pragma unroll 4
-            for (int i = tid; i < nloc; i += kThreads) {
-                const uint32_t key = keys[i];
-                if ((key >> (shift + 8)) == hp) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-            }
-        }
-        __syncthreads();
-        cluster_sync_all();
-        uint32_t hv[CL];   // all remote loads in flight before any use
+// Exclusive prefix sum over the block of one value per thread; returns the total.
+// Uses sh.wcnt.
+__device__ __forceinline__ int block_scan1(int& v, SmallShared& sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
 #pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) hv[r] = ld_dsmem_u32(dsmem_addr(&hist[tid], r));
-        uint32_t all = 0u, low = 0u;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    __syncthreads();   // sh.wcnt free
+    if (lane == 31) sh.wcnt[warp][0] = inc;
+    __syncthreads();
+    int pre = inc - v, total = 0;
 #pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) {
-            all += hv[r];
-            low += r < rank ? hv[r] : 0u;
+    for (int w = 0; w < kWarps; ++w) {
+        pre += w < warp ? sh.wcnt[w][0] : 0;
+        total += sh.wcnt[w][0];
+    }
+    v = pre;
+    return total;
+}
+
+// Candidate lists of the fast selection (after the CTA's keys region in shared memory,
+// at the same offsets in every CTA): this CTA's published candidates (key, logical page,
+// physical page), and all CTAs' candidates gathered in ascending page order (later the
+// kept pages, compacted).
+struct CandList {
+    uint32_t* key;
+    int32_t* logical;
+    int32_t* phys;
+};
+__device__ __forceinline__ CandList cand_list(uint8_t* base) {
+    CandList c;
+    c.key = reinterpret_cast<uint32_t*>(base);
+    c.logical = reinterpret_cast<int32_t*>(base + kCandCap * 4);
+    c.phys = reinterpret_cast<int32_t*>(base + kCandCap * 8);
+    return c;
+}
+
+// One radix pass's cluster step: sums the CTAs' histograms `hist` (256 bins) through
+// DSMEM (hv[r] = CTA r's count of this thread's bin) and finds the bin where the count of
+// keys at or above it first reaches `remaining`, scanning from the top bin down. Leaves in
+// sh: digit, above / above_low / above_own (keys in higher bins: all CTAs, lower-ranked
+// CTAs, this CTA), eq_low / eq_own / inbin (keys in the bin: lower-ranked, own, all).
+template <int CL>
+__device__ __forceinline__ void pick_digit(const uint32_t* hist, int remaining, uint32_t rank, SmallShared& sh,
+                                           uint32_t (&hv)[CL]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (uint32_t r = 0; r < CL; ++r) hv[r] = ld_dsmem_u32(dsmem_addr(&hist[tid], r));   // all in flight
+    uint32_t all = 0u, low = 0u;
+#pragma unroll
+    for (uint32_t r = 0; r < CL; ++r) {
+        all += hv[r];
+        low += r < rank ? hv[r] : 0u;
+    }
+    sh.tot[0][tid] = all;
+    sh.tot[1][tid] = low;
+    sh.tot[2][tid] = hist[tid];
+    __syncthreads();
+    if (warp == 0) {
+        // lane l holds bins 8l .. 8l + 7 of (all CTAs, lower-ranked CTAs, this CTA)
+        int c[3][8], t[3], suf[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const uint4 h0 = *reinterpret_cast<const uint4*>(&sh.tot[k][8 * lane]);
+            const uint4 h1 = *reinterpret_cast<const uint4*>(&sh.tot[k][8 * lane + 4]);
+            c[k][0] = h0.x; c[k][1] = h0.y; c[k][2] = h0.z; c[k][3] = h0.w;
+            c[k][4] = h1.x; c[k][5] = h1.y; c[k][6] = h1.z; c[k][7] = h1.w;
+            t[k] = ((c[k][0] + c[k][1]) + (c[k][2] + c[k][3])) + ((c[k][4] + c[k][5]) + (c[k][6] + c[k][7]));
+            suf[k] = t[k];
         }
-        sh.tot[0][tid] = all;
-        sh.tot[1][tid] = low;
-        sh.tot[2][tid] = hist[tid];
-        __syncthreads();
-        if (warp == 0) {
-            // lane l holds bins 8l .. 8l + 7 of (all CTAs, lower-ranked CTAs, this CTA);
-            // the digit is the bin where the count of keys at or above it first
-            // reaches `remaining`, scanning from the top bin down
-            int c[3][8], t[3], suf[3];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
-                const uint4 h0 = *reinterpret_cast<const uint4*>(&sh.tot[k][8 * lane]);
-                const uint4 h1 = *reinterpret_cast<const uint4*>(&sh.tot[k][8 * lane + 4]);
-                c[k][0] = h0.x; c[k][1] = h0.y; c[k][2] = h0.z; c[k][3] = h0.w;
-                c[k][4] = h1.x; c[k][5] = h1.y; c[k][6] = h1.z; c[k][7] = h1.w;
-                t[k] = ((c[k][0] + c[k][1]) + (c[k][2] + c[k][3])) + ((c[k][4] + c[k][5]) + (c[k][6] + c[k][7]));
-                suf[k] = t[k];
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-                for (int k = 0; k < 3; ++k) {
-                    const int y = __shfl_down_sync(0xffffffffu, suf[k], o);
-                    if (lane + o < 32) suf[k] += y;
-                }
-            }
-            int ab[3];
-#pragma unroll
-            for (int k = 0; k < 3; ++k) ab[k] = suf[k] - t[k];   // keys in the bins of higher lanes
-#pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                if (ab[0] < remaining && ab[0] + c[0][i] >= remaining) {
-                    sh.digit = 8 * lane + i;
-                    sh.above = ab[0];
-                    sh.above_low = ab[1];
-                    sh.above_own = ab[2];
-                    sh.eq_low = c[1][i];
-                    sh.eq_own = c[2][i];
-                    sh.inbin = c[0][i];
-                }
-#pragma unroll
-                for (int k = 0; k < 3; ++k) ab[k] += c[k][i];
+                const int y = __shfl_down_sync(0xffffffffu, suf[k], o);
+                if (lane + o < 32) suf[k] += y;
             }
         }
-        __syncthreads();
-        prefix |= static_cast<uint32_t>(sh.digit) << shift;
+        int ab[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) ab[k] = suf[k] - t[k];   // keys in the bins of higher lanes
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+            if (ab[0] < remaining && ab[0] + c[0][i] >= remaining) {
+                sh.digit = 8 * lane + i;
+                sh.above = ab[0];
+                sh.above_low = ab[1];
+                sh.above_own = ab[2];
+                sh.eq_low = c[1][i];
+                sh.eq_own = c[2][i];
+                sh.inbin = c[0][i];
+            }
+#pragma unroll
+            for (int k = 0; k < 3; ++k) ab[k] += c[k][i];
+        }
+    }
+    __syncthreads();
+}
+
+// The general radix select (kept out of line: the fast candidate path runs otherwise),
+// entered after the first pass over the fast range (its result in sh and sh.bin_cnt).
+// restart: the K-th key lay outside the fast range, so the select starts over as an
+// MSB-first radix over the whole key. Each later pass histograms the next 8 bits of the
+// key's offset from the range's base among the keys matching the digits so far; once the
+// chosen bin holds at most kRankCap keys across the cluster, every CTA publishes its keys
+// of that bin, gathers all of them through DSMEM and ranks them directly. The kept keys
+// are then written by an ordered compaction: the pass counts place each CTA's kept keys
+// in the ascending output without a further exchange.
+template <int CL>
+__device__ __noinline__ int select_general(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int j0, int nloc,
+                                           int K, const uint32_t* keys, SmallShared& sh, RadixRange fr,
+                                           bool restart) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    int32_t* out = a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap;
+    uint32_t base = restart ? 0u : fr.base, pv = 0u;
+    int shift = restart ? 24 : fr.s, prev = 32;
+    int remaining = K;
+    int gt_low = 0, gt_own = 0, eq_low = 0, eq_own = 0;
+    uint32_t T = 0u;
+    bool have = !restart;   // sh holds the result of the pass over (base, shift, prev)
+#pragma unroll 1
+    for (int pass = 1;; ++pass) {
+        uint32_t hv[CL];
+        if (!have) {
+            uint32_t* hist = sh.hist[pass & 1];   // alternating: other CTAs read the previous one
+            hist[tid] = 0u;
+            __syncthreads();
+            if (prev >= 32) {
+                // whole-key first digit (the top byte takes few values): one shared atomic per
+                // distinct bin per warp step
+#pragma unroll 1
+                for (int i0 = 0; i0 < nloc; i0 += kThreads) {
+                    const int i = i0 + tid;
+                    const uint32_t bin = i < nloc ? (keys[i] - base) >> shift : 0xffffffffu;
+                    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                    if (i < nloc && lane == __ffs(peers) - 1)
+                        atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
+                }
+            } else {
+                const uint32_t hp = pv >> prev, mask = (1u << (prev - shift)) - 1u;
+#pragma unroll 1
+                for (int i = tid; i < nloc; i += kThreads) {
+                    const uint32_t v = keys[i] - base;
+                    if ((v >> prev) == hp) atomicAdd(&hist[(v >> shift) & mask], 1u);
+                }
+            }
+            __syncthreads();
+            cluster_sync_all();
+            pick_digit<CL>(hist, remaining, rank, sh, hv);
+            if (tid == sh.digit) {
+#pragma unroll
+                for (uint32_t r = 0; r < CL; ++r) sh.bin_cnt[r] = static_cast<int>(hv[r]);
+            }
+        }
+        have = false;
+        const uint32_t digit = static_cast<uint32_t>(sh.digit);
+        pv |= digit << shift;
         remaining -= sh.above;
         gt_low += sh.above_low;
         gt_own += sh.above_own;
         eq_low = sh.eq_low;
         eq_own = sh.eq_own;
         const int inbin = sh.inbin;
-        if (pass < 3 && inbin <= kRankCap) {
+        if (shift > 0 && inbin <= kRankCap) {
             // The K-th largest key is one of the inbin keys of the chosen bin: every CTA
             // publishes its keys of that bin, every CTA gathers all of them through DSMEM and
             // ranks them directly instead of running the remaining passes.
-            if (tid == sh.digit) {
-#pragma unroll
-                for (uint32_t r = 0; r < CL; ++r) sh.bin_cnt[r] = static_cast<int>(hv[r]);
-            }
             if (tid == 0) sh.nbin = 0;
             __syncthreads();
-            const uint32_t want = prefix >> shift;   // every bit at or above this pass's digit
+            const uint32_t want = pv >> shift;   // every bit of v at or above this pass's digit
+#pragma unroll 1
             for (int i0 = 0; i0 < nloc; i0 += kThreads) {
                 const int i = i0 + tid;
                 const uint32_t key = i < nloc ? keys[i] : 0u;
-                const bool m = i < nloc && (key >> shift) == want;
+                const bool m = i < nloc && ((key - base) >> shift) == want;
                 const unsigned bal = __ballot_sync(0xffffffffu, m);
-                int base = 0;
-                if (lane == 0 && bal) base = atomicAdd(&sh.nbin, __popc(bal));
-                base = __shfl_sync(0xffffffffu, base, 0);
-                if (m) sh.bin_keys[base + __popc(bal & lanemask_lt())] = key;
+                int bpos = 0;
+                if (lane == 0 && bal) bpos = atomicAdd(&sh.nbin, __popc(bal));
+                bpos = __shfl_sync(0xffffffffu, bpos, 0);
+                if (m) sh.bin_keys[bpos + __popc(bal & lanemask_lt())] = key;
             }
             cluster_sync_all();   // every CTA's bin keys are complete and visible
             if (tid < inbin) {
-                int r = 0, base = 0;
+                int r = 0, first = 0;
 #pragma unroll
                 for (int q = 0; q < CL - 1; ++q) {
-                    if (r == q && tid >= base + sh.bin_cnt[q]) {   // past rank q's keys: move on
-                        base += sh.bin_cnt[q];
+                    if (r == q && tid >= first + sh.bin_cnt[q]) {   // past rank q's keys: move on
+                        first += sh.bin_cnt[q];
                         r = q + 1;
                     }
                 }
-                sh.rank_keys[tid] = ld_dsmem_u32(dsmem_addr(&sh.bin_keys[tid - base], static_cast<uint32_t>(r)));
+                sh.rank_keys[tid] = ld_dsmem_u32(dsmem_addr(&sh.bin_keys[tid - first], static_cast<uint32_t>(r)));
                 sh.rank_src[tid] = static_cast<uint8_t>(r);
             }
             if (tid < 4) sh.cnt4[tid] = 0;
@@ -519,6 +882,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
             if (tid < inbin) {
                 const uint32_t key = sh.rank_keys[tid];
                 int gt = 0, ge = 0;
+#pragma unroll 1
                 for (int q = 0; q < inbin; ++q) {
                     const uint32_t v = sh.rank_keys[q];
                     gt += v > key;
@@ -530,7 +894,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
                 }
             }
             __syncthreads();
-            const uint32_t T = sh.rank_T;
+            T = sh.rank_T;
             if (tid < inbin) {
                 const uint32_t key = sh.rank_keys[tid];
                 const int r = sh.rank_src[tid];
@@ -542,25 +906,257 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
             gt_own += sh.cnt4[1];
             eq_low = sh.cnt4[2];
             eq_own = sh.cnt4[3];
-            prefix = T;
             remaining = sh.rank_take;
             break;
         }
+        if (shift == 0) {   // every bit fixed: T is the K-th largest key (ties by page id)
+            T = base + pv;
+            break;
+        }
+        prev = shift;
+        shift = max(0, shift - 8);
     }
-    // T = prefix is the K-th largest key; the first `remaining` keys equal to it are
-    // kept. This CTA keeps its keys > T and its first take_cta keys == T, written from
-    // position pos0 on (the kept keys of lower-ranked CTAs come first).
+    // T is the K-th largest key; the first `remaining` keys equal to it are kept. This CTA
+    // keeps its keys > T and its first take_cta keys == T, written from position pos0 on
+    // (the kept keys of lower-ranked CTAs come first).
     const int take_cta = max(0, min(remaining - eq_low, eq_own));
     const int pos0 = gt_low + min(eq_low, remaining);
-    ordered_keep(keys, nloc, prefix, take_cta, sh, [&](int i, int pos) {
+    ordered_keep(keys, nloc, T, take_cta, sh, [&](int i, int pos) {
         if (pos0 + pos < K) out[pos0 + pos] = j0 + i;   // always < K; the guard only bounds a logic error
     });
     return K;
 }
+
+// Writes selected[b][kvh][0..K) and n_selected[b][kvh]; returns K. When the fast
+// candidate path ran, *listed is set and the kept pages (logical, physical) are in the
+// gathered candidate list, ascending, so the attention needs no further exchange.
+// Cluster-wide radix select: each CTA histograms its own keys and every CTA sums the
+// CTAs' histograms through DSMEM and picks the digit. The first pass takes the fast
+// range (its histogram is built with the keys). If the chosen bin is inside that range
+// and the keys in it and above it are few (<= kCandCap, the bin's <= kRankCap), every
+// CTA publishes those candidate keys (in page order, with their physical pages; the sure
+// ones above the bin also get an L2 prefetch of their K/V), gathers all CTAs' lists
+// through DSMEM after one cluster barrier, ranks the bin's keys directly and keeps the
+// K largest (equal keys by lower page id). Otherwise later passes take the next 8 bits of
+// the key's offset from the range's base, ending, when the chosen bin holds at most
+// kRankCap keys, in a direct ranking of that bin, and the kept keys are written by an
+// ordered compaction (the pass counts place each CTA's kept keys in the output).
+template <int CL, int GM>
+__device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk, uint8_t* big,
+                            SmallShared& sh, bool stage_q, bool* listed) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(big);
+    const CandList pub = cand_list(big + region_a_bytes(chunk));
+    const CandList cand = cand_list(big + region_a_bytes(chunk) + kCandListBytes);
+    *listed = false;
+    const int g = a.hq / a.hkv;
+    // Loads that do not depend on the sequence length go out first: this CTA's nominal page
+    // range [jn0, jn0 + nn) of the score rows (bulk copies into the staging buffer), an L2
+    // prefetch of its page-table entries, and the query rows.
+    const int jn0 = min(a.max_pages, static_cast<int>(rank) * chunk);
+    const int nn = min(chunk, a.max_pages - jn0);
+    const int64_t stride = a.max_pages;
+    const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * stride;
+    const bool vec = (a.max_pages & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
+    // groups of more than four heads read their scores with loads (staging them four rows at
+    // a time would serialise the copies)
+    const bool staged = GM <= kHB && vec && nn > 0 && kHB * chunk * 4 <= kStageBytes;
+    if (tid == 0 && staged) stage_rows(srow, stride, 0, min(g, kHB), jn0, nn, chunk, reinterpret_cast<float*>(keys), sh);
+    if (tid == 32 && nn > 0 && a.page_table && vec && (reinterpret_cast<uintptr_t>(a.page_table) & 15) == 0)
+        prefetch_l2_bulk(a.page_table + static_cast<int64_t>(b) * a.max_pages + jn0,
+                         static_cast<uint32_t>((nn + 3) & ~3) * 4u);
+    float qv[16 * kD / kThreads];
+    if (stage_q) load_query(a, b, kvh, g, qv);
+    const int seq_len = a.seq_pages[b];
+    bool failed = false;
+    if (staged && !a.lse_partials && !mbar_wait_bounded(&sh.sbar, 0, a.st.wait_limit_ns)) failed = true;
+
+    const int P = max(0, min(seq_len, a.max_pages));
+    const int j0 = min(P, jn0);
+    const int j1 = min(P, j0 + chunk);
+    const int nloc = j1 - j0;
+    normaliser<CL, GM>(a, b, kvh, g, j0, j1, staged, reinterpret_cast<float*>(keys), chunk, sh);
+    if (stage_q) store_query(qv, g, sh);   // read after the barriers below
+    int K = min(a.budget_pages, min(P, a.k_cap));
+    K = max(K, 0);
+    const bool select = K > 0 && K < P;
+    const RadixRange fr = fast_range(select ? K : 1, select ? P : 2);
+    if (staged && a.lse_partials && !mbar_wait_bounded(&sh.sbar, 0, a.st.wait_limit_ns)) failed = true;
+    // per-warp histograms of the keys in the (still unused) candidate-list space, zeroed by
+    // the kernel's prologue
+    uint32_t* whist = reinterpret_cast<uint32_t*>(pub.key);
+    group_keys<GM>(a, b, kvh, j0, j1, chunk, keys, sh, staged, fr, select, whist, failed);
+    // the page-table entries of this CTA's pages into the staged score rows that are free now
+    // (rows 1..3; row 0 holds the keys), for the candidates' physical pages
+    int32_t* ptab = reinterpret_cast<int32_t*>(keys) + chunk;
+    const bool paged = a.page_table && a.k_cache && a.v_cache;
+    const bool ptab_staged = vec && paged && nloc > 0 && select && 2 * chunk * 4 <= region_a_bytes(chunk) &&
+                             (reinterpret_cast<uintptr_t>(a.page_table) & 15) == 0;
+    const uint32_t ptab_phase = staged ? 1u : 0u;   // the staging barrier's phases: scores, then this
+    if (ptab_staged && tid == 0) {
+        fence_proxy_async_smem();   // the rows' generic reads (the keys pass) before the async refill
+        const uint32_t bytes = static_cast<uint32_t>((nloc + 3) & ~3) * 4u;
+        mbar_arrive_expect_tx(&sh.sbar, bytes);
+        bulk_g2s(ptab, a.page_table + static_cast<int64_t>(b) * a.max_pages + j0, bytes, &sh.sbar);
+    }
+    if (failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
+
+    int32_t* out = a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap;
+    if (rank == 0 && tid == 0) a.n_selected[b * a.hkv + kvh] = K;
+    if (K == 0) return 0;
+    if (K == P) {
+        for (int j = j0 + tid; j < j1; j += kThreads) out[j] = j;
+        return K;
+    }
+
+    // pass 0 over the fast range (its histogram was built with the keys)
+    cluster_sync_all();
+    uint32_t hv[CL];
+    pick_digit<CL>(sh.hist[0], K, rank, sh, hv);
+    const uint32_t digit = static_cast<uint32_t>(sh.digit);
+    if (tid == static_cast<int>(digit)) {
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) sh.bin_cnt[r] = static_cast<int>(hv[r]);
+    }
+    const int remaining = K - sh.above, inbin = sh.inbin;
+    if (digit == 0u || digit == 255u || inbin > kRankCap || K - remaining + inbin > kCandCap) {
+        // the staged page-table copy lands before that space is reused
+        if (ptab_staged && !mbar_wait_bounded(&sh.sbar, ptab_phase & 1u, a.st.wait_limit_ns))
+            report_error(a.st, LOCKS_ERR_TIMEOUT);
+        __syncthreads();
+        return select_general<CL>(a, b, kvh, rank, j0, nloc, K, keys, sh, fr, digit == 0u || digit == 255u);
+    }
+
+    // ---- fast candidate path
+    const uint32_t lo_u = fr.base + (digit << fr.s);   // first key image of the chosen bin
+    const uint64_t hi_u = static_cast<uint64_t>(fr.base) + (static_cast<uint64_t>(digit + 1) << fr.s);
+    const int64_t kv_row = static_cast<int64_t>(kPage) * kD * 2;   // bytes per (page, kv head)
+    // publish this CTA's candidates (keys >= lo_u) in page order by an ordered compaction,
+    // then their physical pages (from the staged page-table entries) and an L2 prefetch of
+    // the K/V of those above the bin, which are kept for sure (selection-only launches carry
+    // no table or caches)
+    bool pt_failed = ptab_staged && !mbar_wait_bounded(&sh.sbar, ptab_phase & 1u, a.st.wait_limit_ns);
+    if (pt_failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
+    const int npub = ordered_keep(keys, nloc, lo_u - 1u, 0, sh, [&](int i, int pos) {
+        if (pos < kCandCap) {   // always: the count was checked; the guard bounds a logic error
+            pub.key[pos] = keys[i];
+            pub.logical[pos] = j0 + i;
+        }
+    });
+    __syncthreads();
+#pragma unroll 1
+    for (int t = tid; t < min(npub, kCandCap); t += kThreads) {
+        int phys = 0;
+        if (paged) {
+            const int i = pub.logical[t] - j0;
+            phys = ptab_staged ? ptab[i] : a.page_table[static_cast<int64_t>(b) * a.max_pages + j0 + i];
+            if (phys < 0 || phys >= a.num_phys) {
+                report_error(a.st, LOCKS_ERR_BAD_INDEX);
+                phys = 0;
+            }
+            if (static_cast<uint64_t>(pub.key[t]) >= hi_u) {
+                const int64_t unit = static_cast<int64_t>(phys) * a.hkv + kvh;
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.k_cache) + unit * kv_row, kv_row);
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.v_cache) + unit * kv_row, kv_row);
+            }
+        }
+        pub.phys[t] = phys;
+    }
+    if (tid == 0) sh.pub_n = npub;
+    cluster_sync_all();   // every CTA's list is complete and visible
+    if (tid < CL) sh.cnt_r[tid] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.pub_n, tid)));
+    __syncthreads();
+    int off[CL + 1];
+    off[0] = 0;
+#pragma unroll
+    for (int r = 0; r < CL; ++r) off[r + 1] = off[r] + sh.cnt_r[r];
+    const int N = min(off[CL], kCandCap);
+    // gather: element i of the ascending list, from the CTA whose range holds it
+    uint32_t ck[3];
+    int cl[3], cp[3], eqf[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int i = 3 * tid + u;
+        ck[u] = 0u;
+        cl[u] = cp[u] = 0;
+        if (i < N) {
+            int r = 0, first = 0;
+#pragma unroll
+            for (int q = 1; q < CL; ++q)
+                if (i >= off[q]) {
+                    r = q;
+                    first = off[q];
+                }
+            const int k = i - first;
+            ck[u] = ld_dsmem_u32(dsmem_addr(&pub.key[k], static_cast<uint32_t>(r)));
+            cl[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.logical[k], static_cast<uint32_t>(r))));
+            cp[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.phys[k], static_cast<uint32_t>(r))));
+        }
+    }
+    // the bin's keys, unordered, for the ranking
+    if (tid == 0) sh.nbin = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const bool m = 3 * tid + u < N && static_cast<uint64_t>(ck[u]) < hi_u;
+        const unsigned bal = __ballot_sync(0xffffffffu, m);
+        int bpos = 0;
+        if (lane == 0 && bal) bpos = atomicAdd(&sh.nbin, __popc(bal));
+        bpos = __shfl_sync(0xffffffffu, bpos, 0);
+        if (m) sh.rank_keys[bpos + __popc(bal & lanemask_lt())] = ck[u];
+    }
+    __syncthreads();
+    const int nb = min(sh.nbin, kRankCap);
+    if (tid < nb) {
+        const uint32_t key = sh.rank_keys[tid];
+        int gt = 0, ge = 0;
+#pragma unroll 8
+        for (int q = 0; q < nb; ++q) {
+            const uint32_t v = sh.rank_keys[q];
+            gt += v > key;
+            ge += v >= key;
+        }
+        if (gt < remaining && ge >= remaining) {   // key is the remaining-th largest of the bin
+            sh.rank_T = key;
+            sh.rank_take = remaining - gt;
+        }
+    }
+    __syncthreads();
+    const uint32_t T = sh.rank_T;
+    const int take = sh.rank_take;
+    // kept: every key > T, and the first `take` keys == T in page order
+#pragma unroll
+    for (int u = 0; u < 3; ++u) eqf[u] = (3 * tid + u < N && ck[u] == T) ? 1 : 0;
+    block_scan3(eqf, sh);
+    int kf[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) kf[u] = (3 * tid + u < N && (ck[u] > T || (ck[u] == T && eqf[u] < take))) ? 1 : 0;
+    block_scan3(kf, sh);   // kf -> output positions
+    // the kept list (ascending) into the gathered-list arrays; this CTA writes its share of
+    // selected[]
+    const int share = (K + CL - 1) / CL;
+    const int s0 = static_cast<int>(rank) * share, s1 = min(K, s0 + share);
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int i = 3 * tid + u;
+        const bool keep = i < N && (ck[u] > T || (ck[u] == T && eqf[u] < take));
+        if (keep && kf[u] < kCandCap) {
+            cand.logical[kf[u]] = cl[u];
+            cand.phys[kf[u]] = cp[u];
+            if (kf[u] >= s0 && kf[u] < s1) out[kf[u]] = cl[u];
+        }
+    }
+    *listed = true;
+    __syncthreads();
+    return K;
+}
 // ------------------------------------------------------------- attention
+// Pages come from `sel` (global, logical ids, looked up through the page table), or, when
+// list_log is given, from lists in shared memory of (logical, physical) pages.
 template <int CL, int GM>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
-                             const int32_t* sel, bool sel_coherent, bool q_staged, uint8_t* ring, SmallShared& sh) {
+                             const int32_t* sel, bool sel_coherent, bool q_staged, uint8_t* ring, SmallShared& sh,
+                             const int32_t* list_log = nullptr, const int32_t* list_phys = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, t = lane & 3;
     const int g = a.hq / a.hkv;
@@ -606,12 +1202,14 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     for (int p = p0 + warp; p < p1; p += kWarps) {
         // tokens of the page that are attended
         const int valid = p < n_sel ? kPage : min(kPage, tail - (p - n_sel) * kPage);
-        int logical = p < n_sel ? (sel_coherent ? __ldcg(sel + p) : sel[p]) : tail_page + (p - n_sel);
+        const bool listed = list_log && p < n_sel;
+        int logical = p < n_sel ? (listed ? list_log[p] : (sel_coherent ? __ldcg(sel + p) : sel[p]))
+                                : tail_page + (p - n_sel);
         if (logical < 0 || logical >= a.max_pages) {
             bad = true;
             logical = 0;
         }
-        int64_t phys = a.page_table[static_cast<int64_t>(b) * a.max_pages + logical];
+        int64_t phys = listed ? list_phys[p] : a.page_table[static_cast<int64_t>(b) * a.max_pages + logical];
         if (phys < 0 || phys >= a.num_phys) {
             bad = true;
             phys = 0;
@@ -720,19 +1318,30 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     {
         float* ra = wpart + (warp * kMaxG + gid) * kPartStride;
         float* rb = wpart + (warp * kMaxG + gid + 8) * kPartStride;
-        if (t == 0) {
-            ra[0] = m_a;
-            ra[1] = l_a;
-            rb[0] = m_b;
-            rb[1] = l_b;
-        }
+        // rows of heads >= g hold nothing and are never read
+        if (gid < g) {
+            if (t == 0) {
+                ra[0] = m_a;
+                ra[1] = l_a;
+            }
 #pragma unroll
-        for (int nd = 0; nd < 16; ++nd) {
-            const int d = 8 * nd + 2 * t;
-            ra[2 + d] = o[nd][0];
-            ra[2 + d + 1] = o[nd][1];
-            rb[2 + d] = o[nd][2];
-            rb[2 + d + 1] = o[nd][3];
+            for (int nd = 0; nd < 16; ++nd) {
+                const int d = 8 * nd + 2 * t;
+                ra[2 + d] = o[nd][0];
+                ra[2 + d + 1] = o[nd][1];
+            }
+        }
+        if (gid + 8 < g) {
+            if (t == 0) {
+                rb[0] = m_b;
+                rb[1] = l_b;
+            }
+#pragma unroll
+            for (int nd = 0; nd < 16; ++nd) {
+                const int d = 8 * nd + 2 * t;
+                rb[2 + d] = o[nd][2];
+                rb[2 + d + 1] = o[nd][3];
+            }
         }
     }
     __syncthreads();
@@ -848,6 +1457,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     // of this grid has started; it waits for this grid's completion itself
     allow_dependent_launch();
     if (threadIdx.x < kWarps) mbar_init(&sh.bar[threadIdx.x], 1);
+    if (threadIdx.x == kWarps) mbar_init(&sh.sbar, 1);
+    if constexpr (MODE != SAMode::kAttend) {
+        // the selection's per-warp key histograms (in the candidate-list space)
+        uint32_t* whist = reinterpret_cast<uint32_t*>(big + region_a_bytes(chunk));
+        static_assert(kWarps * 256 * 4 <= kCandListBytes, "per-warp histograms fit a candidate list");
+#pragma unroll 1
+        for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) whist[i] = 0u;
+    }
     fence_barrier_init();
     // launched with programmatic stream serialization: the set-up above overlaps
     // the end of the previous kernel (the scorer); every global access follows
@@ -855,19 +1472,25 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     __syncthreads();
 
     if constexpr (MODE == SAMode::kSelect) {
-        select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh, false);
+        bool listed = false;
+        select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, false, &listed);
         cluster_sync_all();   // this CTA's shared data stays readable until every CTA is done with it
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
         attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, false,
                              false, big, sh);
     } else {
-        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, reinterpret_cast<uint32_t*>(big), sh, true);
-        // the selection went to global memory; make it visible to the cluster's CTAs
-        asm volatile("fence.acq_rel.cluster;" ::: "memory");
-        cluster_sync_all();
+        bool listed = false;
+        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, true, &listed);
+        if (!listed) {
+            // the selection went to global memory; make it visible to the cluster's CTAs
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            cluster_sync_all();
+        }
+        // fast selection: every CTA holds the kept pages, ascending, in its gathered list
+        const CandList kept = cand_list(big + region_a_bytes(chunk) + kCandListBytes);
         attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, true,
-                             true, big, sh);
+                             true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr);
     }
 }
 
@@ -990,9 +1613,8 @@ int active_clusters_cl(size_t smem, SAMode mode) {
 
 size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode) {
     const size_t small = sizeof(SmallShared) + 1024;   // + alignment of the region after it
-    const size_t keys = (mode == SAMode::kAttend) ? 0 : static_cast<size_t>(chunk_of(max_pages, cluster)) * 4;
-    const size_t ring = (mode == SAMode::kSelect) ? 0 : static_cast<size_t>(kRingBytes);
-    return small + (keys > ring ? keys : ring);
+    if (mode == SAMode::kAttend) return small + static_cast<size_t>(kRingBytes);
+    return small + static_cast<size_t>(region_a_bytes(chunk_of(max_pages, cluster))) + 2 * kCandListBytes;
 }
 
 int group_bound(int g) { return g <= 4 ? 4 : 16; }

@@ -92,6 +92,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             "locks_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "locks_k_cap": ([D, I32, ctypes.POINTER(I32)], ctypes.c_int),
             "locks_workspace_size": ([D, I32, ctypes.POINTER(S)], ctypes.c_int),
+            "locks_lse_partials_size": ([D, ctypes.POINTER(S)], ctypes.c_int),
             "locks_build_summaries": ([D, P, P, I32, SUM, P, S, P], ctypes.c_int),
             "locks_score_pages": ([D, P, SUM, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_select_pages": ([D, P, P, P, I32, P, P, P, P, S, P], ctypes.c_int),
@@ -212,9 +213,15 @@ def locks_build_summaries(dims, k_cache, phys_page_ids, n_pages, summaries: Summ
         _stream(stream)))
 
 
+def locks_lse_partials_size(dims: locks_dims_t) -> int:
+    n = ctypes.c_size_t(0)
+    _check("locks_lse_partials_size", load_library().locks_lse_partials_size(ctypes.byref(dims), ctypes.byref(n)))
+    return int(n.value)
+
+
 def lse_partials_shape(dims: locks_dims_t):
-    """Shape of the optional LSE-partials buffer (fp32 pairs per 8-page block)."""
-    return (dims.batch, dims.num_q_heads, (dims.max_pages_per_seq + 7) // 8, 2)
+    """Shape of an fp32 tensor holding the optional LSE-partials buffer."""
+    return (locks_lse_partials_size(dims) // 4,)
 
 
 def locks_score_pages(dims, q, summaries: Summaries, page_table, seq_pages, scores, workspace=None,

@@ -52,7 +52,8 @@ def test_status_strings_and_sizes(lib):
     assert lib.locks_k_cap(dims, 15) == 1
     assert lib.locks_k_cap(lib.make_dims(1, 1, 1, 10, 10), 2048) == 10
     ws = lib.locks_workspace_size(dims, 2048)
-    need = 2 * 32 * 1000 * 4 + 2 * 32 * 125 * 8 + 2 * 8 * 128 * 4 + 2 * 8 * 4
+    need = 2 * 32 * 1000 * 4 + 2 * 32 * 256 * 2 * 8 + 2 * 8 * 128 * 4 + 2 * 8 * 4   # scores, partials, selection
+    assert lib.locks_lse_partials_size(dims) == 2 * 32 * 256 * 2 * 8
     assert need <= ws <= need + 5 * 256
 
 
@@ -88,16 +89,17 @@ def test_host_validation_codes(lib):
 
 def test_noalloc_rejects_oversized_problems_on_the_host(lib):
     """The workspace-free decode step refuses, before any CUDA call, a problem whose
-    scratch exceeds its fixed 36 MiB array (batch 4 x 32 heads x 1M tokens needs 40 MiB)."""
+    scratch exceeds its fixed 36 MiB array (batch 5 x 32 heads x 1M tokens needs 40.6 MiB)."""
     so = lib.load_library()
     fn = so.locks_decode_step_noalloc
     P = ctypes.c_void_p
     fn.argtypes = [ctypes.POINTER(lib.locks_dims_t), P, P, P, lib.locks_summaries_t, P, P, ctypes.c_int32, P, P, P]
     fn.restype = ctypes.c_int
     S = lib.locks_summaries_t(None, None, None, None)
-    for dims, budget in ((lib.make_dims(4, 32, 2, 65536, 4 * 65536), 512),
-                         (lib.make_dims(4, 32, 8, 65536, 4 * 65536), 2048)):
+    for dims, budget in ((lib.make_dims(5, 32, 2, 65536, 5 * 65536), 512),
+                         (lib.make_dims(5, 32, 8, 65536, 5 * 65536), 2048)):
         assert lib.locks_workspace_size(dims, budget) > (36 << 20)
         assert fn(ctypes.byref(dims), None, None, None, S, None, None, budget, None, None, None) == \
             lib.LOCKS_ERR_WORKSPACE_TOO_SMALL
-    assert lib.locks_workspace_size(lib.make_dims(3, 32, 8, 65536, 3 * 65536), 2048) <= (36 << 20)
+    assert lib.locks_workspace_size(lib.make_dims(4, 32, 8, 65536, 4 * 65536), 2048) <= (36 << 20)
+    assert lib.locks_workspace_size(lib.make_dims(4, 32, 2, 65536, 4 * 65536), 512) <= (36 << 20)

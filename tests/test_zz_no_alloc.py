@@ -121,13 +121,14 @@ def test_noalloc_at_the_largest_fitting_table():
     assert rc == L.LOCKS_ERR_WORKSPACE_TOO_SMALL
 
 
-def test_noalloc_rejects_the_4x1m_workload():
-    """Batch 4 at 32 query heads x 65536 pages needs 40 MiB of scratch: rejected."""
+def test_noalloc_size_limit_at_1m_context():
+    """At 32 query heads and 1M tokens batch 4 fits the array (the 4 x 1M GLM-shaped
+    workload included) and batch 5 is rejected before anything is launched."""
     fn = _noalloc_fn()
-    dims = L.make_dims(4, 32, 2, 65536, 4 * 65536)
-    assert L.locks_workspace_size(dims, 512) > SCRATCH_BYTES
-    rc = fn(ctypes.byref(dims), None, None, None, L.locks_summaries_t(None, None, None, None), None, None, 512,
-            None, None, None)
-    assert rc == L.LOCKS_ERR_WORKSPACE_TOO_SMALL
-    dims = L.make_dims(3, 32, 8, 65536, 3 * 65536)
-    assert L.locks_workspace_size(dims, 2048) <= SCRATCH_BYTES
+    for hkv, budget in ((8, 2048), (2, 512)):
+        assert L.locks_workspace_size(L.make_dims(4, 32, hkv, 65536, 4 * 65536), budget) <= SCRATCH_BYTES
+        dims = L.make_dims(5, 32, hkv, 65536, 5 * 65536)
+        assert L.locks_workspace_size(dims, budget) > SCRATCH_BYTES
+        rc = fn(ctypes.byref(dims), None, None, None, L.locks_summaries_t(None, None, None, None), None, None,
+                budget, None, None, None)
+        assert rc == L.LOCKS_ERR_WORKSPACE_TOO_SMALL
