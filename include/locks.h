@@ -205,8 +205,8 @@ LOCKS_API int locks_score_pages(const locks_dims_t* dims, const float* q, locks_
  * n_selected[b][kvh] = k. sel_keys (fp32 [B][Hkv][max_pages_per_seq], may be
  * NULL) receives key_j for j < seq_pages[b]. lse_partials (may be NULL) are
  * the partials locks_score_pages wrote for these same scores and dims on this
- * device; when given, L_h is reduced from them. A NaN score carries no mass (it is
- * read as -inf), so a page whose group scores are all NaN ranks last.
+ * device; when given, L_h is reduced from them. A NaN score adds nothing to L_h and
+ * gives its page a NaN key, which ranks last.
  */
 LOCKS_API int locks_select_pages(const locks_dims_t* dims, const float* scores, const float* lse_partials,
                                  const int32_t* seq_pages, int32_t budget_tokens, int32_t* selected,
