@@ -198,6 +198,11 @@ def algorithmic_bytes(w: synth.Workload, budget: int) -> tuple[int, int]:
     return units * UNIT_BYTES, w.batch * w.num_kv_heads * k * PAGE_KV_BYTES
 
 
+def units_of(w: synth.Workload) -> int:
+    """(physical page, kv head) units of the workload's cache."""
+    return w.num_phys_pages * w.num_kv_heads
+
+
 def config_of(w: synth.Workload, budget: int) -> dict:
     return {"workload": f"{w.name}: {w.description}", "batch": w.batch, "context_tokens": w.context,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": 16,
@@ -487,17 +492,43 @@ def run_locks(args, rank, world, local):
     e2e_value = reduce_max(statistics.mean(e2e_us), world, dev)
     e2e_eager = reduce_max(statistics.mean(e2e_eager_us), world, dev)
 
-    # full-model decode graph (outside the timed region): 32 layers' decode steps (score +
-    # select_attend each) in one CUDA graph, each layer streaming the same resident buffers
-    # (far larger than L2, so every layer reads its summaries and K/V from HBM)
+    # full-model decode graph (outside the timed region): 32 layers' decode steps
+    # (locks_decode_step each) in one CUDA graph, every layer with its own query, K/V cache,
+    # summaries, workspace and outputs (the page table is shared, as one block table serves
+    # every layer). The caches hold N(0,1) bf16 keys and values drawn on the device and the
+    # summaries are built from them; as many distinct layers as fit in 60% of the free
+    # memory, layer i using set i mod n_distinct.
     model_graph = None
     if not args.no_model_graph:
         n_layers = 32
+        kv_bytes_layer = 2 * kc.numel() * 2
+        per_layer = kv_bytes_layer + units_of(w) * UNIT_BYTES + L.locks_workspace_size(dims, budget) + (1 << 20)
+        free = torch.cuda.mem_get_info(dev)[0]
+        n_distinct = max(2, min(n_layers, int(0.6 * free // per_layer)))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(4321)
+        sets = []
+        for i in range(n_distinct):
+            kc_i = torch.randn(tuple(kc.shape), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+            vc_i = torch.randn(tuple(vc.shape), generator=gen, device=dev, dtype=torch.bfloat16).view(torch.int16)
+            summ_i = L.Summaries.empty(w.num_phys_pages, w.num_kv_heads, dev)
+            L.locks_build_summaries(dims, kc_i, ids, w.num_phys_pages, summ_i)
+            sets.append(dict(q=torch.randn(tuple(q.shape), generator=gen, device=dev), kc=kc_i, vc=vc_i,
+                             summ=summ_i, ws=L.alloc_workspace(dims, budget, dev), out=torch.empty_like(out),
+                             lse=torch.empty_like(lse)))
+        torch.cuda.synchronize()
+
+        def model_step():
+            for layer in range(n_layers):
+                z = sets[layer % n_distinct]
+                L.locks_decode_step(dims, z["q"], z["kc"], z["vc"], z["summ"], table, seq, budget, z["out"],
+                                    z["ws"], lse=z["lse"])
+
+        model_step()
+        torch.cuda.synchronize()
         g_model = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_model):
-            for _ in range(n_layers):
-                score()
-                select_attend()
+            model_step()
         g_model.replay()
         torch.cuda.synchronize()
         m_us = []
@@ -511,13 +542,18 @@ def run_locks(args, rank, world, local):
             if i >= 1:
                 m_us.append(a_.elapsed_time(b_) * 1000.0)
         model_us = reduce_max(statistics.mean(m_us), world, dev)
-        model_graph = {"layers": n_layers, "us": model_us, "per_layer_us": model_us / n_layers,
+        model_graph = {"layers": n_layers, "distinct_layer_sets": n_distinct, "us": model_us,
+                       "per_layer_us": model_us / n_layers,
                        "per_layer_vs_single_step": (model_us / n_layers) / mean_step_us, "replays": len(m_us),
-                       "path": "32 x (score_pages, select_attend) captured in one CUDA graph on the same "
-                               "buffers, L2 flushed before each replay; the summaries stream from HBM in "
-                               "every layer, the selected K/V pages (k x 8 KiB per kv head) of one layer "
-                               "can stay in L2 for the next, which separate layers' caches would not"}
-        assert L.locks_get_device_status(ws) == 0, "device status after the model graph"
+                       "path": f"32 x locks_decode_step captured in one CUDA graph, L2 flushed before each "
+                               f"replay; each layer has its own query, K/V cache (N(0,1) bf16 drawn on the "
+                               f"device), summaries built from it, workspace and outputs: {n_distinct} distinct "
+                               f"sets, layer i using set i mod {n_distinct} (layers sharing a set are "
+                               f"{n_distinct} apart); the page table is shared by every layer"}
+        for z in sets:
+            assert L.locks_get_device_status(z["ws"]) == 0, "device status after the model graph"
+        del sets
+        torch.cuda.empty_cache()
 
     # page-fill refresh (outside the timed region): the one-page summary build a filled page
     # needs, alone and overlapped with a decode step on a second stream
