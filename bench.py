@@ -380,6 +380,24 @@ def run_locks(args, rank, world, local):
     torch.cuda.synchronize()
     build_ms = e0.elapsed_time(e1)
 
+    # the summary build at the GLM-4-9B-shaped 4 x 1M configuration (262,144 pages x 2 kv
+    # heads of N(0,1) bf16 keys drawn on the device), timed as prefill pages/s
+    glm = synth.WORKLOADS["glm9b_4x1m"]
+    glm_pages = glm.batch * glm.pages
+    glm_dims = L.make_dims(glm.batch, glm.num_q_heads, glm.num_kv_heads, glm.pages, glm_pages)
+    gk = torch.randn((glm_pages, glm.num_kv_heads, 16, 128), device=dev, dtype=torch.bfloat16).view(torch.int16)
+    gsumm = L.Summaries.empty(glm_pages, glm.num_kv_heads, dev)
+    gids = torch.arange(glm_pages, dtype=torch.int32, device=dev)
+    L.locks_build_summaries(glm_dims, gk, gids, glm_pages, gsumm)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    L.locks_build_summaries(glm_dims, gk, gids, glm_pages, gsumm)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    glm_build_ms = e0.elapsed_time(e1)
+    del gk, gsumm, gids
+    torch.cuda.empty_cache()
+
     k_cap = L.locks_k_cap(dims, budget)
     ws = L.alloc_workspace(dims, budget, dev)
     scores = torch.empty((w.batch, w.num_q_heads, w.pages), dtype=torch.float32, device=dev)
@@ -696,6 +714,16 @@ def run_locks(args, rank, world, local):
                      "algorithmic_bytes_per_launch": summ_bytes, "units_per_launch": units,
                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                      "traffic_source": traffic["source"] if traffic else None},
+        "roofline_select_attend": {
+            "kernel": "select_attend (the decode step's second launch: group keys, top-k, sparse attention)",
+            "bound": "hbm", "achieved": kv_bytes / (mean_sa_us * 1e-6) / 1e9, "peak": hbm,
+            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+            "frac": kv_bytes / (mean_sa_us * 1e-6) / 1e9 / hbm,
+            "algorithmic_bytes_per_launch": kv_bytes,
+            "algorithmic_bytes": "selected K/V: 8 KiB per kept (page, kv head)",
+            "l2_resident_bytes_per_launch": w.batch * w.num_q_heads * w.pages * 4 + L.locks_lse_partials_size(dims),
+            "l2_resident_bytes": "the score table and LSE partials the scorer just wrote (read from L2)",
+            "traffic": None},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "us", "h2d_bytes_per_step": int(q_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host.numel() * 2),
@@ -709,7 +737,11 @@ def run_locks(args, rank, world, local):
         "clocks": clocks, "gpu_launches": 2 * K, "device_status": status,
         "timed_wall_s": wall,
         "build": {"units": units, "ms": build_ms, "pages_per_s": w.batch * w.pages / (build_ms * 1e-3),
-                  "units_per_s": units / (build_ms * 1e-3)},
+                  "units_per_s": units / (build_ms * 1e-3),
+                  "glm9b_4x1m_prefill": {"pages": glm_pages, "kv_heads": glm.num_kv_heads, "ms": glm_build_ms,
+                                         "pages_per_s": glm_pages / (glm_build_ms * 1e-3),
+                                         "units_per_s": glm_pages * glm.num_kv_heads / (glm_build_ms * 1e-3),
+                                         "keys": "N(0,1) bf16 drawn on the device"}},
     }
     print(json.dumps(line), flush=True)
 

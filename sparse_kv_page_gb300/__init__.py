@@ -7,17 +7,17 @@ The compute lives in ``liblocks_gb300.so`` (``csrc/``, declared in
 
 from .locks import (LocksError, Summaries, alloc_ablation_workspace, alloc_workspace, library_path, load_library,
                     locks_ablation_workspace_size, locks_build_summaries, locks_clear_device_status,
-                    locks_decode_step, locks_dims_t, locks_exact_scores, locks_get_device_status, locks_k_cap,
-                    locks_score_pages, locks_select_attend, locks_select_pages, locks_selftest_bounded_wait,
-                    locks_set_wait_limit_ns, locks_shared_basis, locks_shared_scores, locks_sparse_attention,
-                    locks_status_string, locks_summaries_t, locks_variant_scores, locks_version,
-                    locks_workspace_size, make_dims)
+                    locks_decode_step, locks_decode_step_noalloc, locks_dims_t, locks_exact_scores,
+                    locks_get_device_status, locks_k_cap, locks_lse_partials_size, locks_score_pages,
+                    locks_select_attend, locks_select_pages, locks_selftest_bounded_wait, locks_set_wait_limit_ns,
+                    locks_shared_basis, locks_shared_scores, locks_sparse_attention, locks_status_string,
+                    locks_summaries_t, locks_variant_scores, locks_version, locks_workspace_size, make_dims)
 
 __all__ = [
     "LocksError", "Summaries", "alloc_ablation_workspace", "alloc_workspace", "locks_ablation_workspace_size",
     "locks_exact_scores", "locks_shared_basis", "locks_shared_scores", "locks_variant_scores", "library_path", "load_library", "locks_build_summaries",
-    "locks_clear_device_status", "locks_decode_step", "locks_dims_t", "locks_get_device_status", "locks_k_cap",
+    "locks_clear_device_status", "locks_decode_step", "locks_decode_step_noalloc", "locks_dims_t", "locks_get_device_status", "locks_k_cap",
     "locks_score_pages", "locks_select_attend", "locks_select_pages", "locks_selftest_bounded_wait",
     "locks_set_wait_limit_ns", "locks_sparse_attention", "locks_status_string", "locks_summaries_t",
-    "locks_version", "locks_workspace_size", "make_dims",
+    "locks_lse_partials_size", "locks_version", "locks_workspace_size", "make_dims",
 ]

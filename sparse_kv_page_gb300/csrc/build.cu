@@ -13,8 +13,9 @@
 //   quantisation to int8 / int4 / int8 with fp16 scales, packed in the
 //   scorer's fragment order (see include/locks.h).
 //
-// GPU mapping: a warp builds two units at a time. The Gram matrix runs on the
-// tensor cores (f16 hi/lo split of the power-of-two-normalised deviations,
+// GPU mapping: a warp builds two units at a time (three CTAs of four warps per SM; the
+// keys stay in bf16 in shared memory and the deviations are formed on the fly). The Gram
+// matrix runs on the tensor cores (f16 hi/lo split of the power-of-two-normalised deviations,
 // three MMAs per tile, fp32 accumulate); the Jacobi sweeps keep one row of G
 // and one row of the eigenvector matrix per lane (lanes 0-15: first unit,
 // 16-31: second), 8 disjoint rotations per round, 15 rounds per sweep, all
@@ -26,11 +27,14 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kDStride = 136;   // fp32 row stride of D in shared memory (conflict-free float2)
+constexpr int kKStride = 136;   // bf16 row stride of the keys in shared memory (conflict-free fragments)
 constexpr int kMaxSweeps = 10;
+constexpr int kCtasPerSm = 3;   // 12 warps per SM at 168 registers (the shared memory allows it)
 
+// The keys stay in bf16 (exact) and D = K - mu is formed on the fly in fp32, which keeps
+// the per-warp footprint small enough for three CTAs per SM.
 struct WarpSmem {
-    float d[2][kPage * kDStride];
+    uint16_t k[2][kPage * kKStride];
     float mu[2][kD];
     float g[2][kPage * kPage];
     float u8[2][kPage * kRank];
@@ -68,25 +72,16 @@ __device__ __forceinline__ void schur(float app, float aqq, float apq, float& c,
 
 template <int R>
 __device__ __forceinline__ void jacobi_round(float (&gr)[16], float (&ur)[16], int i, int base) {
-    // this lane's pair (p, q) of the round: its diagonal entry and a_pq
+    // this lane's partner in the round ((R, 15), and the indices summing to 2R mod 15),
+    // its diagonal entry and a_pq
+    int partner = (2 * R - i + 15) % 15;
+    partner = i == 15 ? R : (i == R ? 15 : partner);
+    const bool is_p = i < partner;
     float dmine = 0.f, doff = 0.f;
-    int partner = i;
-    bool is_p = true;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int P = pair_p(R, k), Q = pair_q(R, k);
-        if (i == P) {
-            dmine = gr[P];
-            doff = gr[Q];
-            partner = Q;
-            is_p = true;
-        }
-        if (i == Q) {
-            dmine = gr[Q];
-            doff = gr[P];
-            partner = P;
-            is_p = false;
-        }
+    for (int m = 0; m < 16; ++m) {
+        dmine = m == i ? gr[m] : dmine;
+        doff = m == partner ? gr[m] : doff;
     }
     const float dother = __shfl_sync(0xffffffffu, dmine, base + partner);
     const float apq = __shfl_sync(0xffffffffu, doff, base + (is_p ? i : partner));   // both lanes use row p's
@@ -142,56 +137,52 @@ __device__ __forceinline__ int quant(float x, float s, int qmax) {
     return static_cast<int>(c);
 }
 
-// Loads a unit's keys, centres them, and forms the Gram matrix in w.g[slot].
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Loads a unit's keys (bf16, kept as they are), their mean mu, and the Gram matrix of the
+// centred keys D = K - mu into w.g[slot].
 __device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, int slot, int lane) {
-    float* d = w.d[slot];
+    uint16_t* k = w.k[slot];
     float* mu = w.mu[slot];
     const int gid = lane >> 2, t = lane & 3;
     if (unit >= 0) {
         const uint16_t* src =
             a.k_cache + (static_cast<int64_t>(a.phys_page_ids[unit / a.hkv]) * a.hkv + unit % a.hkv) * (kPage * kD);
+        uint4 v[8];   // all of this lane's loads in flight
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int c = lane + 32 * m;
-            const int row = c >> 4, col = (c & 15) * 8;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + row * kD + col);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            float* dst = d + row * kDStride + col;
+            v[m] = *reinterpret_cast<const uint4*>(src + (c >> 4) * kD + (c & 15) * 8);
+        }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                dst[2 * e] = __uint_as_float(wv[e] << 16);
-                dst[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
-            }
+        for (int m = 0; m < 8; ++m) {
+            const int c = lane + 32 * m;
+            *reinterpret_cast<uint4*>(k + (c >> 4) * kKStride + (c & 15) * 8) = v[m];
         }
     } else {
-        for (int idx = lane; idx < kPage * kD; idx += 32) d[(idx / kD) * kDStride + idx % kD] = 0.f;
+        for (int idx = lane; idx < kPage * kD; idx += 32) k[(idx / kD) * kKStride + idx % kD] = 0;
     }
     __syncwarp();
     // mean over the 16 keys, lane -> dims 4 lane .. 4 lane + 3
-    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < kPage; ++i) {
-        const float4 v = *reinterpret_cast<const float4*>(d + i * kDStride + 4 * lane);
-        s4.x += v.x;
-        s4.y += v.y;
-        s4.z += v.z;
-        s4.w += v.w;
+        const uint2 v = *reinterpret_cast<const uint2*>(k + i * kKStride + 4 * lane);
+        s4[0] += bf16_lo(v.x);
+        s4[1] += bf16_hi(v.x);
+        s4[2] += bf16_lo(v.y);
+        s4[3] += bf16_hi(v.y);
     }
-    s4.x *= (1.f / kPage);
-    s4.y *= (1.f / kPage);
-    s4.z *= (1.f / kPage);
-    s4.w *= (1.f / kPage);
-    *reinterpret_cast<float4*>(mu + 4 * lane) = s4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s4[q] *= (1.f / kPage);
+    *reinterpret_cast<float4*>(mu + 4 * lane) = make_float4(s4[0], s4[1], s4[2], s4[3]);
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < kPage; ++i) {
-        float4 v = *reinterpret_cast<const float4*>(d + i * kDStride + 4 * lane);
-        v.x -= s4.x;
-        v.y -= s4.y;
-        v.z -= s4.z;
-        v.w -= s4.w;
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        *reinterpret_cast<float4*>(d + i * kDStride + 4 * lane) = v;
+        const uint2 v = *reinterpret_cast<const uint2*>(k + i * kKStride + 4 * lane);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x) - s4[0]), fabsf(bf16_hi(v.x) - s4[1])),
+                                 fmaxf(fabsf(bf16_lo(v.y) - s4[2]), fabsf(bf16_hi(v.y) - s4[3]))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -209,8 +200,10 @@ __device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, 
         for (int r = 0; r < 4; ++r) {
             const int row = gid + ((r & 1) ? 8 : 0);
             const int col = 16 * s + 2 * t + ((r & 2) ? 8 : 0);
-            const float2 x = *reinterpret_cast<const float2*>(d + row * kDStride + col);
-            const uint32_t p0 = split_f16_hilo(x.x * inv), p1 = split_f16_hilo(x.y * inv);
+            const uint32_t kv = *reinterpret_cast<const uint32_t*>(k + row * kKStride + col);
+            const float2 m2 = *reinterpret_cast<const float2*>(mu + col);
+            const uint32_t p0 = split_f16_hilo((bf16_lo(kv) - m2.x) * inv);
+            const uint32_t p1 = split_f16_hilo((bf16_hi(kv) - m2.y) * inv);
             hi[r] = __byte_perm(p0, p1, 0x5410);
             lo[r] = __byte_perm(p0, p1, 0x7632);
         }
@@ -298,9 +291,10 @@ __device__ void jacobi_top8(WarpSmem& w, int lane) {
 
 // V, C, quantisation and packing for one unit; writes its summary bytes.
 __device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int slot, int lane) {
-    const float* d = w.d[slot];
+    const uint16_t* k = w.k[slot];
     const float* u8 = w.u8[slot];
     const float* sig = w.sig[slot];
+    const float4 mu4 = *reinterpret_cast<const float4*>(w.mu[slot] + 4 * lane);
     // V[d][r] = sum_i D[i][d] u_r[i] / sigma_r, lane -> dims 4 lane .. +3
     float v[4][kRank];
 #pragma unroll
@@ -309,11 +303,12 @@ __device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int s
         for (int r = 0; r < kRank; ++r) v[q][r] = 0.f;
 #pragma unroll
     for (int i = 0; i < kPage; ++i) {
-        const float4 dv = *reinterpret_cast<const float4*>(d + i * kDStride + 4 * lane);
+        const uint2 kv = *reinterpret_cast<const uint2*>(k + i * kKStride + 4 * lane);
         const float4 ua = *reinterpret_cast<const float4*>(u8 + i * kRank);
         const float4 ub = *reinterpret_cast<const float4*>(u8 + i * kRank + 4);
         const float uu[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-        const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
+        const float dd[4] = {bf16_lo(kv.x) - mu4.x, bf16_hi(kv.x) - mu4.y, bf16_lo(kv.y) - mu4.z,
+                             bf16_hi(kv.y) - mu4.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -454,7 +449,7 @@ __device__ __forceinline__ int64_t valid_unit(const BuildArgs& a, int64_t u) {
     return u;
 }
 
-__global__ void __launch_bounds__(kThreads) build_kernel(BuildArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) build_kernel(BuildArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WarpSmem& w = reinterpret_cast<WarpSmem*>(smem)[warp];
@@ -482,7 +477,7 @@ cudaError_t launch_build(const BuildArgs& a, int num_sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t pairs = (n_units + 1) / 2;
     int64_t grid = (pairs + kWarps - 1) / kWarps;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 2;
+    const int64_t cap = static_cast<int64_t>(num_sms) * kCtasPerSm;
     if (grid > cap) grid = cap;
     build_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
     return cudaGetLastError();

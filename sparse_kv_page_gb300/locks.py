@@ -101,6 +101,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             "locks_decode_step": ([D, P, P, P, SUM, P, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_select_attend_tail": ([D, P, P, P, P, P, P, P, P, I32, P, P, P, P, P, S, P], ctypes.c_int),
             "locks_decode_step_tail": ([D, P, P, P, SUM, P, P, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
+            "locks_decode_step_noalloc": ([D, P, P, P, SUM, P, P, I32, P, P, P], ctypes.c_int),
             "locks_get_device_status": ([P, ctypes.POINTER(I32), P], ctypes.c_int),
             "locks_clear_device_status": ([P, P], ctypes.c_int),
             "locks_set_wait_limit_ns": ([U64], ctypes.c_int),
@@ -282,6 +283,15 @@ def locks_decode_step(dims, q, k_cache, v_cache, summaries: Summaries, page_tabl
             ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), summaries.c(), _ptr(page_table),
             _ptr(seq_pages), _ptr(tail_tokens), int(budget_tokens), _ptr(out), _ptr(lse), _ptr(scores),
             _ptr(selected), _ptr(n_selected), ws, nws, _stream(stream)))
+
+
+def locks_decode_step_noalloc(dims, q, k_cache, v_cache, summaries: Summaries, page_table, seq_pages,
+                              budget_tokens, out, lse=None, stream=None) -> None:
+    """locks_decode_step with the library's fixed scratch array in place of a workspace, for
+    callers that cannot allocate device memory (see include/locks.h)."""
+    _check("locks_decode_step_noalloc", load_library().locks_decode_step_noalloc(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), summaries.c(), _ptr(page_table),
+        _ptr(seq_pages), int(budget_tokens), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def locks_get_device_status(workspace, stream=None) -> int:
