@@ -18,8 +18,9 @@
 // matrix runs on the tensor cores (f16 hi/lo split of the power-of-two-normalised deviations,
 // three MMAs per tile, fp32 accumulate); the Jacobi sweeps keep one row of G
 // and one row of the eigenvector matrix per lane (lanes 0-15: first unit,
-// 16-31: second), 8 disjoint rotations per round, 15 rounds per sweep, all
-// indices static (fully unrolled), operands exchanged with warp shuffles.
+// 16-31: second), 8 disjoint rotations per round on fixed position pairs followed by
+// the round-robin permutation of positions, 15 rounds per sweep, register indices
+// static, operands exchanged with warp shuffles; the round loop stays rolled.
 #include "locks_internal.h"
 
 namespace locks {
@@ -43,89 +44,87 @@ struct WarpSmem {
     int8_t ccode[kPage * kRank];
 };
 
-// Round-robin pairing of 16 indices: round r pairs (r, 15) and
-// ((r + k) mod 15, (r - k) mod 15), k = 1..7.
-__host__ __device__ constexpr int pair_p(int r, int k) {
-    return k == 0 ? r : ((r + k) % 15 < (r - k + 15) % 15 ? (r + k) % 15 : (r - k + 15) % 15);
-}
-__host__ __device__ constexpr int pair_q(int r, int k) {
-    return k == 0 ? 15 : ((r + k) % 15 < (r - k + 15) % 15 ? (r - k + 15) % 15 : (r + k) % 15);
-}
-
-// Symmetric Schur rotation that zeroes a_pq (Golub & Van Loan, section 8.5).
+// Symmetric Schur rotation that zeroes a_pq (Golub & Van Loan, section 8.5). The
+// quotients may be approximate: c = 1/sqrt(1 + t^2) and s = t c form an orthogonal
+// rotation for any t, and t only steers how much of a_pq it removes.
 __device__ __forceinline__ void schur(float app, float aqq, float apq, float& c, float& s) {
     if (fabsf(apq) <= 1e-30f || fabsf(apq) <= 1e-9f * sqrtf(fabsf(app * aqq))) {
         c = 1.f;
         s = 0.f;
         return;
     }
-    const float tau = (aqq - app) / (2.f * apq);
+    const float tau = __fdividef(aqq - app, 2.f * apq);
     float t;
     if (fabsf(tau) > 1e18f) {
-        t = 0.5f / tau;
+        t = __fdividef(0.5f, tau);
     } else {
-        t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+        t = __fdividef(tau >= 0.f ? 1.f : -1.f, fabsf(tau) + sqrtf(1.f + tau * tau));
     }
     c = rsqrtf(1.f + t * t);
     s = t * c;
 }
 
-template <int R>
+// Parallel ordering of the cyclic Jacobi method (the round-robin "circle" schedule): every
+// round rotates the fixed position pairs (2k, 2k + 1), then the positions are permuted --
+// position 0 stays, the others move one step around the circle of top positions 2k and
+// bottom positions 2k + 1 -- so that in 15 rounds every pair of indices meets once. After a
+// round position i holds what position rr_src(i) held before.
+__host__ __device__ constexpr int rr_src(int i) {
+    return i == 0 ? 0 : (i == 2 ? 1 : (i == 15 ? 14 : ((i & 1) ? i + 2 : i - 2)));
+}
+
+// One round on a half-warp's matrix: lane i (within the half, base = first lane of the
+// half) holds row i of G (gr) and row i of U (ur), columns in registers. Every round runs
+// the same code, so the round loop stays rolled and its instructions cached.
 __device__ __forceinline__ void jacobi_round(float (&gr)[16], float (&ur)[16], int i, int base) {
-    // this lane's partner in the round ((R, 15), and the indices summing to 2R mod 15),
-    // its diagonal entry and a_pq
-    int partner = (2 * R - i + 15) % 15;
-    partner = i == 15 ? R : (i == R ? 15 : partner);
-    const bool is_p = i < partner;
+    const bool is_p = (i & 1) == 0;   // pair (p, q) = (2k, 2k + 1)
     float dmine = 0.f, doff = 0.f;
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         dmine = m == i ? gr[m] : dmine;
-        doff = m == partner ? gr[m] : doff;
+        doff = m == (i ^ 1) ? gr[m] : doff;
     }
-    const float dother = __shfl_sync(0xffffffffu, dmine, base + partner);
-    const float apq = __shfl_sync(0xffffffffu, doff, base + (is_p ? i : partner));   // both lanes use row p's
+    const float dother = __shfl_sync(0xffffffffu, dmine, base + (i ^ 1));
+    const float apq = __shfl_sync(0xffffffffu, doff, base + (i & ~1));   // both lanes use row p's
     float cm, sm;
     schur(is_p ? dmine : dother, is_p ? dother : dmine, apq, cm, sm);
     // every lane needs every pair's rotation for the column update
     float c[8], s[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        c[k] = __shfl_sync(0xffffffffu, cm, base + pair_p(R, k));
-        s[k] = __shfl_sync(0xffffffffu, sm, base + pair_p(R, k));
+        c[k] = __shfl_sync(0xffffffffu, cm, base + 2 * k);
+        s[k] = __shfl_sync(0xffffffffu, sm, base + 2 * k);
     }
-    // G <- G J and U <- U J (columns p, q of this lane's rows)
+    // G <- G J and U <- U J (columns 2k, 2k + 1 of this lane's rows)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const int P = pair_p(R, k), Q = pair_q(R, k);
-        const float gp = gr[P], gq = gr[Q];
-        gr[P] = c[k] * gp - s[k] * gq;
-        gr[Q] = s[k] * gp + c[k] * gq;
-        const float up = ur[P], uq = ur[Q];
-        ur[P] = c[k] * up - s[k] * uq;
-        ur[Q] = s[k] * up + c[k] * uq;
+        const float gp = gr[2 * k], gq = gr[2 * k + 1];
+        gr[2 * k] = c[k] * gp - s[k] * gq;
+        gr[2 * k + 1] = s[k] * gp + c[k] * gq;
+        const float up = ur[2 * k], uq = ur[2 * k + 1];
+        ur[2 * k] = c[k] * up - s[k] * uq;
+        ur[2 * k + 1] = s[k] * up + c[k] * uq;
     }
     // G <- J^T G (rows p, q): combine with the partner row
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        const float other = __shfl_sync(0xffffffffu, gr[m], base + partner);
+        const float other = __shfl_sync(0xffffffffu, gr[m], base + (i ^ 1));
         gr[m] = is_p ? (cm * gr[m] - sm * other) : (sm * other + cm * gr[m]);
     }
-}
-
-template <int... Rs>
-struct Rounds;
-template <>
-struct Rounds<> {
-    __device__ static void run(float (&)[16], float (&)[16], int, int) {}
-};
-template <int R0, int... Rs>
-struct Rounds<R0, Rs...> {
-    __device__ static void run(float (&gr)[16], float (&ur)[16], int i, int base) {
-        jacobi_round<R0>(gr, ur, i, base);
-        Rounds<Rs...>::run(gr, ur, i, base);
+    // the round-robin permutation: columns of G and U in registers, rows of G across lanes
+    float tg[16], tu[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        tg[m] = gr[rr_src(m)];
+        tu[m] = ur[rr_src(m)];
     }
-};
+    const int src = base + rr_src(i);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        gr[m] = __shfl_sync(0xffffffffu, tg[m], src);
+        ur[m] = tu[m];
+    }
+}
 
 __device__ __forceinline__ float f16_round_scale(float amax, float qmax) {
     return __half2float(__float2half_rn(amax / qmax));
@@ -244,6 +243,7 @@ __device__ void jacobi_top8(WarpSmem& w, int lane) {
     for (int m = 0; m < 16; ++m) fro2 += gr[m] * gr[m];
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) fro2 += __shfl_xor_sync(0xffffffffu, fro2, o);
+    float prev_off2 = INFINITY;
 #pragma unroll 1
     for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
         float off2 = 0.f, dg = 0.f;
@@ -255,9 +255,13 @@ __device__ void jacobi_top8(WarpSmem& w, int lane) {
         off2 -= dg * dg;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) off2 += __shfl_xor_sync(0xffffffffu, off2, o);
-        const bool done = off2 <= 1e-10f * fro2;   // off-diagonal <= 1e-5 ||G||: below int4 resolution
+        // converged: off-diagonal energy <= 1e-10 ||G||^2 (below int4 resolution), or
+        // <= 1e-6 ||G||^2 and no longer halving per sweep (the fp32 rounding floor)
+        const bool done = off2 <= 1e-10f * fro2 || (off2 <= 1e-6f * fro2 && off2 > 0.5f * prev_off2);
+        prev_off2 = off2;
         if (__all_sync(0xffffffffu, done)) break;
-        Rounds<0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14>::run(gr, ur, i, base);
+#pragma unroll 1
+        for (int r = 0; r < 15; ++r) jacobi_round(gr, ur, i, base);
     }
     float lam = 0.f;
 #pragma unroll
