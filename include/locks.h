@@ -347,6 +347,21 @@ LOCKS_API int locks_clear_device_status(void* workspace, void* stream);
 LOCKS_API int locks_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Tuning and testing control (no counterpart on the LOCKS pages): pins the
+ * thread-block cluster size of every later selection and attention launch from
+ * this process (locks_select_pages, locks_sparse_attention, locks_select_attend,
+ * locks_decode_step and their variants) to 8, 12 or 16 CTAs; 0 restores the
+ * automatic choice. A 12-CTA cluster runs one CTA per SM; 8- and 16-CTA
+ * clusters may run two. An attention-only launch that splits a long selection
+ * over several clusters still picks its own size. Any other value returns
+ * LOCKS_ERR_INVALID_ARG and changes nothing. A size whose shared memory does not
+ * fit makes those launches return LOCKS_ERR_CUDA. The selection does not depend
+ * on the size; the attention output does only through rounding (the share of
+ * pages each warp accumulates). Host-side setting, read at launch time.
+ */
+LOCKS_API int locks_set_select_cluster(int32_t cluster);
+
+/*
  * Failure-detection self test (no counterpart on the LOCKS pages): launches
  * one CTA that waits on an mbarrier phase nothing will complete. The wait
  * gives up after limit_ns and records LOCKS_ERR_TIMEOUT in the status word of

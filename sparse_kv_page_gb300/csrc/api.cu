@@ -35,53 +35,67 @@ int num_sms(int dev) {
     return v;
 }
 
-// Cluster size (16 or 8) for the select/attend kernels. A cluster of CL CTAs
-// handles one (sequence, kv head) segment; when the segments do not all fit
-// at once the launch runs in waves, so the choice minimises
-// waves x (pages per CTA + a fixed per-CTA cost in page units). Residency
-// counts come from the occupancy API, cached per (device, mode, group, pages).
-// Co-resident 16- and 8-CTA clusters of the select/attend kernel (occupancy API),
-// cached per (device, mode, group bound, pages).
-void active_clusters(int dev, const locks_dims_t* d, locks::SAMode mode, int* a16_out, int* a8_out) {
+// Cluster size for the select/attend kernels: 16 or 8 (two CTAs of either share an SM when
+// their shared memory allows, and the hardware then packs them so), or 12 (one CTA per
+// SM). A cluster of CL CTAs handles one (sequence, kv head) segment; when the segments do
+// not all fit at once the launch runs in waves, so the choice minimises
+// waves x (pages per SM + a fixed per-CTA cost in page units), for the selection launch's
+// shared memory. Attention-only launches that do not split take the same size, so that
+// they divide a selection among CTAs and warps as the fused launch does. Residency counts
+// come from the occupancy API, cached per (device, mode, group bound, pages).
+// locks_set_select_cluster pins the size.
+std::atomic<int> g_select_cluster{0};
+constexpr int kClusterSizes[3] = {16, 12, 8};
+
+struct ClusterFit {
+    int active[3];    // co-resident clusters, per kClusterSizes entry (0: cannot launch)
+    int per_sm[3];    // CTAs of the launch sharing an SM
+};
+
+ClusterFit cluster_fit(int dev, const locks_dims_t* d, locks::SAMode mode) {
     struct Entry {
         int dev, mode, gbound, max_pages;
-        int active16, active8;
+        ClusterFit fit;
     };
     static std::mutex mu;
     static Entry table[128];
     static int n = 0;
     const int g = d->num_q_heads / d->num_kv_heads;
     const int gbound = g <= 4 ? 4 : 16;
-    int a16 = -1, a8 = -1;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < n; ++i)
-            if (table[i].dev == dev && table[i].mode == static_cast<int>(mode) && table[i].gbound == gbound &&
-                table[i].max_pages == d->max_pages_per_seq) {
-                a16 = table[i].active16;
-                a8 = table[i].active8;
-                break;
-            }
-        if (a16 < 0) {
-            a16 = locks::select_attend_active_clusters(d->max_pages_per_seq, mode, g, 16);
-            a8 = locks::select_attend_active_clusters(d->max_pages_per_seq, mode, g, 8);
-            if (n < 128) table[n++] = {dev, static_cast<int>(mode), gbound, d->max_pages_per_seq, a16, a8};
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (table[i].dev == dev && table[i].mode == static_cast<int>(mode) && table[i].gbound == gbound &&
+            table[i].max_pages == d->max_pages_per_seq)
+            return table[i].fit;
+    ClusterFit f;
+    for (int i = 0; i < 3; ++i) {
+        const int cl = kClusterSizes[i];
+        f.active[i] = locks::select_attend_active_clusters(d->max_pages_per_seq, mode, g, cl);
+        f.per_sm[i] = locks::select_attend_ctas_per_sm(d->max_pages_per_seq, mode, cl);
     }
-    *a16_out = a16;
-    *a8_out = a8;
+    if (n < 128) table[n++] = {dev, static_cast<int>(mode), gbound, d->max_pages_per_seq, f};
+    return f;
 }
 
-int cluster_size(int dev, const locks_dims_t* d, locks::SAMode mode) {
-    int a16 = 0, a8 = 0;
-    active_clusters(dev, d, mode, &a16, &a8);
+int cluster_size(int dev, const locks_dims_t* d) {
+    const int pinned = g_select_cluster.load();
+    if (pinned != 0) return pinned;
+    const ClusterFit f = cluster_fit(dev, d, locks::SAMode::kSelectAttend);
     const long segs = static_cast<long>(d->batch) * d->num_kv_heads;
-    auto cost = [&](int cl, int active) -> double {
-        if (active <= 0) return 1e30;
-        const long waves = (segs + active - 1) / active;
-        return static_cast<double>(waves) * ((d->max_pages_per_seq + cl - 1) / cl + 2048.0);
-    };
-    return cost(16, a16) <= cost(8, a8) ? 16 : 8;
+    int best = 16;
+    double best_cost = 1e300;
+    for (int i = 0; i < 3; ++i) {
+        if (f.active[i] <= 0) continue;
+        const int cl = kClusterSizes[i];
+        const long waves = (segs + f.active[i] - 1) / f.active[i];
+        const double cost = static_cast<double>(waves) *
+                            (static_cast<double>(f.per_sm[i]) * ((d->max_pages_per_seq + cl - 1) / cl) + 2048.0);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = cl;
+        }
+    }
+    return best;
 }
 
 locks::DeviceStatus status_of(void* ws) {
@@ -154,15 +168,14 @@ WsLayout ws_layout(const locks_dims_t* d, int32_t budget) {
 // keeps at least kMinSplitPages pages; otherwise one cluster per segment.
 constexpr int kMinSplitPages = 64;
 void attention_plan(int dev, const locks_dims_t* d, int k_cap, bool can_split, int* cl, int* splits) {
-    *cl = cluster_size(dev, d, locks::SAMode::kAttend);
+    *cl = cluster_size(dev, d);
     *splits = 1;
     if (!can_split) return;
-    int a16 = 0, a8 = 0;
-    active_clusters(dev, d, locks::SAMode::kAttend, &a16, &a8);
+    const ClusterFit f = cluster_fit(dev, d, locks::SAMode::kAttend);
     const long segs = static_cast<long>(d->batch) * d->num_kv_heads;
     long best = *cl;
     for (int c : {16, 8}) {
-        const long act = c == 16 ? a16 : a8;
+        const long act = c == 16 ? f.active[0] : f.active[2];
         long sp = std::min<long>(locks::kMaxSplits, act / std::max<long>(segs, 1));
         sp = std::min<long>(sp, k_cap / (static_cast<long>(c) * kMinSplitPages));
         if (sp >= 2 && c * sp > best) {
@@ -257,7 +270,7 @@ int select_attend_impl(const locks_dims_t* dims, const float* q, const uint16_t*
     a.tail_tokens = tail_tokens;
     a.out = out;
     a.lse = lse;
-    const int cl = cluster_size(dev, dims, locks::SAMode::kSelectAttend);
+    const int cl = cluster_size(dev, dims);
     return cuda_status(locks::launch_select_attend(a, locks::SAMode::kSelectAttend, cl, st));
 }
 
@@ -304,6 +317,12 @@ int locks_lse_partials_size(const locks_dims_t* dims, size_t* bytes) {
 
 int locks_set_wait_limit_ns(uint64_t ns) {
     g_wait_limit_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+    return LOCKS_OK;
+}
+
+int locks_set_select_cluster(int32_t cluster) {
+    if (cluster != 0 && cluster != 8 && cluster != 12 && cluster != 16) return LOCKS_ERR_INVALID_ARG;
+    g_select_cluster.store(cluster);
     return LOCKS_OK;
 }
 
@@ -370,7 +389,7 @@ int locks_select_pages(const locks_dims_t* dims, const float* scores, const floa
     a.sel_keys = sel_keys;
     a.budget_pages = budget_tokens / LOCKS_PAGE_SIZE;
     a.k_cap = k_cap_of(dims, budget_tokens);
-    const int cl = cluster_size(dev, dims, locks::SAMode::kSelect);
+    const int cl = cluster_size(dev, dims);
     return cuda_status(locks::launch_select_attend(a, locks::SAMode::kSelect, cl, static_cast<cudaStream_t>(stream)));
 }
 

@@ -101,9 +101,11 @@ enum class SAMode { kSelect, kAttend, kSelectAttend };
 constexpr int kMaxSplits = 4;
 constexpr int kSplitPartFloats = 2 + 128;   // m, l, o[128] per (b, q head, split)
 cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream);
-// Clusters of `cluster` CTAs (8 or 16) of the select/attend kernel that can be
-// resident at once on the current device (0 if it cannot launch).
+// Clusters of `cluster` CTAs (8, 12 or 16; 12 runs one CTA per SM) of the select/attend
+// kernel that can be resident at once on the current device (0 if it cannot launch), and
+// how many of its CTAs share an SM (1 or 2, from shared memory).
 int select_attend_active_clusters(int max_pages, SAMode mode, int group, int cluster);
+int select_attend_ctas_per_sm(int max_pages, SAMode mode, int cluster);
 size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode);
 
 struct BuildArgs {

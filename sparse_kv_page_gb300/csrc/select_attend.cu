@@ -27,6 +27,7 @@
 // normaliser L_h is reduced from them instead of from the full score table.
 // At most 128 registers per thread so that two CTAs share an SM.
 #include <cudaTypedefs.h>
+#include <algorithm>
 #include <climits>
 #include <cstring>
 
@@ -55,10 +56,30 @@ constexpr int kCandCap = 768;                         // fast selection: candida
 constexpr int kCandListBytes = kCandCap * 12;         // a list of (key, logical page, physical page)
 constexpr int kStageBytes = 64 * 1024;                // staged score rows (four heads) of a CTA's pages
 static_assert(kStageBytes <= kRingBytes, "the staged scores share the attention ring's space");
-// Shared memory after SmallShared: region A (the keys, which overlay the staged score rows,
-// then the attention ring), then (selection) the published and the gathered candidate lists.
-__host__ __device__ constexpr int region_a_bytes(int chunk) {
-    return ((chunk * 4 + 1023) / 1024 * 1024) > kRingBytes ? (chunk * 4 + 1023) / 1024 * 1024 : kRingBytes;
+// The 12-CTA cluster runs one CTA per SM: its launch asks for more shared memory than two
+// CTAs can share. Eight such clusters are co-resident on this GPU (96 SMs), where eight
+// 16-CTA clusters are packed two CTAs to an SM on 64 SMs. Its CTAs may stage up to
+// 128 KiB of score rows (four heads of 8192 pages).
+constexpr int kSpreadCluster = 12;
+constexpr int kSpreadStageBytes = 128 * 1024;
+constexpr int kSpreadSmemBytes = 120 * 1024;
+__host__ __device__ constexpr int stage_cap(int cl) { return cl == kSpreadCluster ? kSpreadStageBytes : kStageBytes; }
+__host__ __device__ constexpr int round_kib(int bytes) { return (bytes + 1023) / 1024 * 1024; }
+// Attention ring: one page slot per warp, two for the 12-CTA cluster (a warp's next page
+// is in flight while it attends the current one).
+__host__ __device__ constexpr int slots_per_warp(int cl) { return cl == kSpreadCluster ? 2 : 1; }
+__host__ __device__ constexpr int ring_bytes(int cl) {
+    return round_kib(slots_per_warp(cl) * kWarps * kPageSlotBytes > kWarpPartBytes
+                         ? slots_per_warp(cl) * kWarps * kPageSlotBytes
+                         : kWarpPartBytes);
+}
+// Shared memory after SmallShared: region A (the keys, which overlay the staged score rows
+// of four heads, then the attention ring), then (selection) the published and the gathered
+// candidate lists.
+__host__ __device__ constexpr int region_a_bytes(int chunk, int cl) {
+    return (4 * chunk * 4 <= stage_cap(cl) && round_kib(4 * chunk * 4) > ring_bytes(cl)) ? round_kib(4 * chunk * 4)
+           : round_kib(chunk * 4) > ring_bytes(cl)                                        ? round_kib(chunk * 4)
+                                                                                           : ring_bytes(cl);
 }
 
 struct SmallShared {
@@ -71,11 +92,12 @@ struct SmallShared {
     int wcnt[kWarps][2];
     int digit, above, above_low, above_own, eq_low, eq_own, inbin;
     // radix early exit: the chosen bin's keys (this CTA's, then all CTAs')
-    int bin_cnt[16], nbin, rank_take, cnt4[4];
+    int bin_cnt[16], nbin, rank_take, rank_eq, cnt4[4];
+    int wtot[3][kWarps];                  // strided scans: flagged elements per (slot, warp)
     uint32_t rank_T;
     uint32_t bin_keys[256], rank_keys[256];
     uint8_t rank_src[256];
-    uint64_t bar[kWarps];
+    uint64_t bar[2 * kWarps];             // attention ring slots (two per warp at most)
     uint64_t sbar;                        // staged score rows (selection)
     int pub_n;                            // fast selection: this CTA's published candidates
     int cnt_r[16];                        // ... and every CTA's count
@@ -180,11 +202,6 @@ __device__ __forceinline__ float round_val(const ScoreRound& x, int i, int hh, i
     return j + e < j1 ? no_nan(s) : -INFINITY;
 }
 
-__device__ __forceinline__ void lse_combine_safe(float& m, float& l, float m2, float l2) {
-    if (!(l2 > 0.f) || m2 == -INFINITY || m2 != m2) return;   // empty or corrupt partial
-    lse_combine(m, l, m2, l2);
-}
-
 // The first radix digit of the selection (fast path). Keys are log mass shares that sum
 // to 1 over the sequence (each head's shares sum to 1 and a key is the group mean), so at
 // most K - 1 keys exceed -ln K, and the K-th largest lies above -ln P (P pages; the mean
@@ -219,9 +236,11 @@ __device__ __forceinline__ RadixRange fast_range(int K, int P) {
     return r;
 }
 __device__ __forceinline__ uint32_t fast_digit(uint32_t u, const RadixRange& r) {
-    if (u < r.base) return 0u;
-    if (u > r.last) return 255u;
-    return (u - r.base) >> r.s;
+    return u < r.base ? 0u : min((u - r.base) >> r.s, 255u);   // above the range: bin 255
+}
+// The float key of an order-preserving image (orderable_key's inverse; image 0 gives NaN).
+__device__ __forceinline__ float key_of_image(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
 
 // Per-head normaliser L_h of sequence b into sh.Lh[0..g) (the same in every CTA).
@@ -425,6 +444,13 @@ __device__ __forceinline__ float comp(const float4& v, int e) {
     return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
 
+// Warp w's share [w0, w1) of a CTA's n keys: contiguous, a multiple of 4 long.
+__device__ __forceinline__ void warp_span(int n, int w, int& w0, int& w1) {
+    const int per = ((n + kWarps - 1) / kWarps + 3) & ~3;
+    w0 = min(n, w * per);
+    w1 = min(n, w0 + per);
+}
+
 // The group keys of this CTA's pages [j0, j1) into keys[] (order-preserving uint32 images)
 // and, when hist0, the fast first radix pass's histogram of them into sh.hist[0] (zeroed
 // by the caller), from sh.Lh. In the log2 domain x_h = s_h log2 e - L_h log2 e <= 0 and
@@ -463,7 +489,78 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
         }
         return u;
     };
-    if constexpr (GM <= kHB) {
+    if (GM <= kHB && staged) {
+        // staged rows: warp w takes the pages of warp_span, lane l the slabs of 4 pages at
+        // 4 l, 4 l + 128, ... of them (so warp w's histogram counts exactly that range);
+        // shared memory by window address, the histogram by shared reductions; the rare
+        // underflow and the optional key output are handled after the loop
+        const uint32_t s_base = smem_u32(stg);
+        const uint32_t wh = smem_u32(whist) + static_cast<uint32_t>(threadIdx.x >> 5) * 1024u;
+        int w0, w1;
+        warp_span(nloc, threadIdx.x >> 5, w0, w1);
+        bool uf = false;
+#pragma unroll 1
+        for (int jj = w0 + 4 * (tid & 31); jj < w1; jj += 128) {
+            float4 v[kHB];
+#pragma unroll
+            for (int hh = 0; hh < kHB; ++hh) {
+                // rows past the group are not staged: read (inside the region) and ignored
+                v[hh] = lds_f4(s_base + static_cast<uint32_t>(hh * chunk + jj) * 4u);
+                if (hh >= g) v[hh] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            uint32_t k4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float z = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < kHB; ++hh) z += fast_exp2(fmaf(comp(v[hh], e), kLog2e, -Lp[hh]));
+                uf |= !(z >= 7.9e-31f) && z == z;   // every share below 2^-100 (or none): redone below
+                const uint32_t u = orderable_key(fast_log2(z) * kLn2 - log_g);
+                const uint32_t d = fast_digit(u, fr);
+                red_shared_add_if(hist0 && d != 0u && jj + e < w1, wh + d * 4u, 1u);
+                k4[e] = u;
+            }
+            sts_u4(s_base + static_cast<uint32_t>(jj) * 4u, make_uint4(k4[0], k4[1], k4[2], k4[3]));
+        }
+        if (__syncthreads_or(uf)) {
+            // pages whose sum underflowed: the key again with the largest term factored out,
+            // from the scores in global memory (row 0 is overwritten by the keys)
+#pragma unroll 1
+            for (int jj = w0 + 4 * (tid & 31); jj < w1; jj += 128) {
+#pragma unroll 1
+                for (int e = 0; e < 4 && jj + e < w1; ++e) {
+                    float x[kHB], m = -INFINITY;
+#pragma unroll
+                    for (int hh = 0; hh < kHB; ++hh) {
+                        x[hh] = hh < g ? fmaf(no_nan(__ldcg(srow + hh * stride + j0 + jj + e)), kLog2e, -Lp[hh])
+                                       : -INFINITY;
+                        m = fmaxf(m, x[hh]);
+                    }
+                    float z = 0.f, zz = 0.f;
+#pragma unroll
+                    for (int hh = 0; hh < kHB; ++hh) {
+                        z += fast_exp2(x[hh]);
+                        zz += fast_exp2(x[hh] - m);
+                    }
+                    const uint32_t old_u = keys[jj + e];
+                    if (old_u == 0u || z >= 7.9e-31f) continue;   // NaN key, or no underflow
+                    const float key2 = m == -INFINITY ? -INFINITY : m + fast_log2(zz);
+                    const uint32_t u = orderable_key(key2 * kLn2 - log_g);
+                    if (hist0) {
+                        const uint32_t d0 = fast_digit(old_u, fr), d1 = fast_digit(u, fr);
+                        if (d0 != 0u) atomicSub(&whist[(threadIdx.x >> 5) * 256 + d0], 1u);
+                        if (d1 != 0u) atomicAdd(&whist[(threadIdx.x >> 5) * 256 + d1], 1u);
+                    }
+                    keys[jj + e] = u;
+                }
+            }
+        }
+        if (kout) {
+            __syncthreads();   // every thread's keys final
+#pragma unroll 1
+            for (int i = tid; i < nloc; i += kThreads) kout[j0 + i] = key_of_image(keys[i]);
+        }
+    } else if constexpr (GM <= kHB) {
         // a rolled loop over this thread's slabs (instruction fetch is part of this code's
         // latency: it runs about once per launch), the slab's four pages in parallel
 #pragma unroll 1
@@ -653,54 +750,32 @@ __device__ int ordered_keep(const uint32_t* keys, int n, uint32_t T, int take_eq
     return gt_all + min(eq_all, take_eq);
 }
 
-// Exclusive prefix sums over the block of three values per thread (thread t holds
-// elements 3t .. 3t + 2, in order); returns the total. Uses sh.wcnt.
-__device__ __forceinline__ int block_scan3(int (&v)[3], SmallShared& sh) {
+// Exclusive ranks, in element order, of the flagged elements among three per thread held
+// strided (thread t holds elements t, t + kThreads, t + 2 kThreads). Uses sh.wtot; one
+// barrier.
+__device__ __forceinline__ void scan_strided(const bool (&f)[3], int (&pos)[3], SmallShared& sh) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int own = v[0] + v[1] + v[2];
-    int inc = own;
+    unsigned bal[3];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
+    for (int u = 0; u < 3; ++u) {
+        bal[u] = __ballot_sync(0xffffffffu, f[u]);
+        if (lane == 0) sh.wtot[u][warp] = __popc(bal[u]);
     }
-    __syncthreads();   // sh.wcnt free
-    if (lane == 31) sh.wcnt[warp][0] = inc;
     __syncthreads();
-    int pre = inc - own, total = 0;
+    const unsigned lt = lanemask_lt();
+    int before = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        pre += w < warp ? sh.wcnt[w][0] : 0;
-        total += sh.wcnt[w][0];
-    }
-    const int v0 = v[0], v1 = v[1];
-    v[0] = pre;
-    v[1] = pre + v0;
-    v[2] = pre + v0 + v1;
-    return total;
-}
-
-// Exclusive prefix sum over the block of one value per thread; returns the total.
-// Uses sh.wcnt.
-__device__ __forceinline__ int block_scan1(int& v, SmallShared& sh) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = v;
+    for (int u = 0; u < 3; ++u) {
+        int in_u = 0, low = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = sh.wtot[u][w];
+            in_u += c;
+            low += w < warp ? c : 0;
+        }
+        pos[u] = before + low + __popc(bal[u] & lt);
+        before += in_u;
     }
-    __syncthreads();   // sh.wcnt free
-    if (lane == 31) sh.wcnt[warp][0] = inc;
-    __syncthreads();
-    int pre = inc - v, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        pre += w < warp ? sh.wcnt[w][0] : 0;
-        total += sh.wcnt[w][0];
-    }
-    v = pre;
-    return total;
 }
 
 // Candidate lists of the fast selection (after the CTA's keys region in shared memory,
@@ -718,6 +793,38 @@ __device__ __forceinline__ CandList cand_list(uint8_t* base) {
     c.logical = reinterpret_cast<int32_t*>(base + kCandCap * 4);
     c.phys = reinterpret_cast<int32_t*>(base + kCandCap * 8);
     return c;
+}
+
+// The gather when some CTA published more than its fixed share of slots: element e of the
+// ascending list comes from the CTA whose offset range holds it (the counts read first).
+// Same layout as the fixed-slot gather.
+template <int CL>
+__device__ __forceinline__ void gather_by_offsets(const CandList& pub, SmallShared& sh, uint32_t (&ck)[3],
+                                               int (&cl)[3], int (&cp)[3], bool (&cv)[3]) {
+    const int tid = threadIdx.x;
+    int off[CL + 1];
+    off[0] = 0;
+#pragma unroll
+    for (int r = 0; r < CL; ++r)
+        off[r + 1] = off[r] + static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.pub_n, static_cast<uint32_t>(r))));
+    const int N = min(off[CL], kCandCap);
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int e = tid + u * kThreads;
+        cv[u] = e < N;
+        if (cv[u]) {
+            int r = 0, first = 0;
+#pragma unroll
+            for (int q = 1; q < CL; ++q) {
+                r = e >= off[q] ? q : r;
+                first = e >= off[q] ? off[q] : first;
+            }
+            const int k = e - first;
+            ck[u] = ld_dsmem_u32(dsmem_addr(&pub.key[k], static_cast<uint32_t>(r)));
+            cl[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.logical[k], static_cast<uint32_t>(r))));
+            cp[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.phys[k], static_cast<uint32_t>(r))));
+        }
+    }
 }
 
 // One radix pass's cluster step: sums the CTAs' histograms `hist` (256 bins) through
@@ -946,8 +1053,8 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
                             SmallShared& sh, bool stage_q, bool* listed) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* keys = reinterpret_cast<uint32_t*>(big);
-    const CandList pub = cand_list(big + region_a_bytes(chunk));
-    const CandList cand = cand_list(big + region_a_bytes(chunk) + kCandListBytes);
+    const CandList pub = cand_list(big + region_a_bytes(chunk, CL));
+    const CandList cand = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
     *listed = false;
     const int g = a.hq / a.hkv;
     // Loads that do not depend on the sequence length go out first: this CTA's nominal page
@@ -960,7 +1067,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     const bool vec = (a.max_pages & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
     // groups of more than four heads read their scores with loads (staging them four rows at
     // a time would serialise the copies)
-    const bool staged = GM <= kHB && vec && nn > 0 && kHB * chunk * 4 <= kStageBytes;
+    const bool staged = GM <= kHB && vec && nn > 0 && kHB * chunk * 4 <= stage_cap(CL);
     if (tid == 0 && staged) stage_rows(srow, stride, 0, min(g, kHB), jn0, nn, chunk, reinterpret_cast<float*>(keys), sh);
     if (tid == 32 && nn > 0 && a.page_table && vec && (reinterpret_cast<uintptr_t>(a.page_table) & 15) == 0)
         prefetch_l2_bulk(a.page_table + static_cast<int64_t>(b) * a.max_pages + jn0,
@@ -990,7 +1097,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     // (rows 1..3; row 0 holds the keys), for the candidates' physical pages
     int32_t* ptab = reinterpret_cast<int32_t*>(keys) + chunk;
     const bool paged = a.page_table && a.k_cache && a.v_cache;
-    const bool ptab_staged = vec && paged && nloc > 0 && select && 2 * chunk * 4 <= region_a_bytes(chunk) &&
+    const bool ptab_staged = vec && paged && nloc > 0 && select && 2 * chunk * 4 <= region_a_bytes(chunk, CL) &&
                              (reinterpret_cast<uintptr_t>(a.page_table) & 15) == 0;
     const uint32_t ptab_phase = staged ? 1u : 0u;   // the staging barrier's phases: scores, then this
     if (ptab_staged && tid == 0) {
@@ -1037,75 +1144,159 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     // no table or caches)
     bool pt_failed = ptab_staged && !mbar_wait_bounded(&sh.sbar, ptab_phase & 1u, a.st.wait_limit_ns);
     if (pt_failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
-    const int npub = ordered_keep(keys, nloc, lo_u - 1u, 0, sh, [&](int i, int pos) {
-        if (pos < kCandCap) {   // always: the count was checked; the guard bounds a logic error
-            pub.key[pos] = keys[i];
-            pub.logical[pos] = j0 + i;
+    // a candidate's physical page (the staged page-table entry, or global memory), with an
+    // L2 prefetch of its K/V when it is kept for sure
+    auto phys_of = [&](int i, uint32_t key) -> int {
+        if (!paged) return 0;
+        int phys = ptab_staged ? ptab[i] : a.page_table[static_cast<int64_t>(b) * a.max_pages + j0 + i];
+        if (phys < 0 || phys >= a.num_phys) {
+            report_error(a.st, LOCKS_ERR_BAD_INDEX);
+            phys = 0;
         }
-    });
-    __syncthreads();
+        if (static_cast<uint64_t>(key) >= hi_u) {
+            const int64_t unit = static_cast<int64_t>(phys) * a.hkv + kvh;
+            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.k_cache) + unit * kv_row, kv_row);
+            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.v_cache) + unit * kv_row, kv_row);
+        }
+        return phys;
+    };
+    int npub = 0;
+    if (GM <= kHB && staged) {
+        // warp w computed the keys of warp_span w, so its candidates are counted by its
+        // histogram's bins >= digit; the counts place every warp's candidates, which one
+        // ordered pass over its keys then writes
+        int cnt = 0;
+        for (int d = static_cast<int>(digit) + lane; d < 256; d += 32) cnt += static_cast<int>(whist[warp * 256 + d]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        if (lane == 0) sh.wcnt[warp][0] = cnt;
+        __syncthreads();   // counts visible, and the histograms (under the list) read by every warp
+        int pos = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            pos += w < warp ? sh.wcnt[w][0] : 0;
+            npub += sh.wcnt[w][0];
+        }
+        int w0, w1;
+        warp_span(nloc, warp, w0, w1);
+        const bool pt_direct = paged && ptab_staged;
+        const uint32_t kaddr = smem_u32(keys), paddr = pt_direct ? smem_u32(ptab) : kaddr;
+        const uint32_t pkey = smem_u32(pub.key), plog = smem_u32(pub.logical), pphys = smem_u32(pub.phys);
+        const int32_t* grow = a.page_table ? a.page_table + static_cast<int64_t>(b) * a.max_pages + j0 : nullptr;
+        const unsigned lt = lanemask_lt();
+        const int first = pos;
+        bool bad = false;
+        // straight-line code (predicated loads and stores): a branch into code not yet
+        // fetched would wait on instruction memory
 #pragma unroll 1
-    for (int t = tid; t < min(npub, kCandCap); t += kThreads) {
-        int phys = 0;
-        if (paged) {
-            const int i = pub.logical[t] - j0;
-            phys = ptab_staged ? ptab[i] : a.page_table[static_cast<int64_t>(b) * a.max_pages + j0 + i];
-            if (phys < 0 || phys >= a.num_phys) {
-                report_error(a.st, LOCKS_ERR_BAD_INDEX);
-                phys = 0;
+        for (int i0 = w0; i0 < w1; i0 += 128) {
+            uint32_t key[4], pt[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = min(i0 + 32 * u + lane, w1 - 1);
+                key[u] = lds_u32(kaddr + static_cast<uint32_t>(i) * 4u);
+                pt[u] = lds_u32(paddr + static_cast<uint32_t>(i) * 4u);   // used when staged
+                key[u] = i0 + 32 * u + lane < w1 ? key[u] : 0u;
             }
-            if (static_cast<uint64_t>(pub.key[t]) >= hi_u) {
-                const int64_t unit = static_cast<int64_t>(phys) * a.hkv + kvh;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u + lane;
+                const unsigned bal = __ballot_sync(0xffffffffu, key[u] >= lo_u);   // lo_u > 0: never past w1
+                const int at = pos + __popc(bal & lt);
+                // always below kCandCap (the count was checked); the test bounds a logic error
+                const bool c = key[u] >= lo_u && at < kCandCap;
+                // the physical page from the staged table (from global memory after the loop
+                // otherwise: a conditional global load here slows the whole loop)
+                int phys = pt_direct ? static_cast<int>(pt[u]) : 0;
+                const bool out_of_range = phys < 0 || phys >= a.num_phys;
+                bad |= c && out_of_range;
+                phys = out_of_range ? 0 : phys;
+                const uint32_t slot = static_cast<uint32_t>(min(at, kCandCap - 1)) * 4u;
+                sts_u32_if(c, pkey + slot, key[u]);
+                sts_u32_if(c, plog + slot, static_cast<uint32_t>(j0 + i));
+                sts_u32_if(c, pphys + slot, static_cast<uint32_t>(phys));
+                pos += __popc(bal);
+            }
+        }
+        __syncwarp();
+        if (paged && !ptab_staged) {
+#pragma unroll 1
+            for (int t = first + lane; t < min(pos, kCandCap); t += 32) {
+                int phys = __ldg(grow + (pub.logical[t] - j0));
+                const bool out_of_range = phys < 0 || phys >= a.num_phys;
+                bad |= out_of_range;
+                pub.phys[t] = out_of_range ? 0 : phys;
+            }
+            __syncwarp();
+        }
+        if (bad) report_error(a.st, LOCKS_ERR_BAD_INDEX);
+        // an L2 prefetch of the K/V of this warp's candidates above the bin (kept for sure),
+        // issued by one lane (a bulk prefetch takes one address per instruction)
+        if (paged && lane == 0) {
+#pragma unroll 1
+            for (int t = first; t < min(pos, kCandCap); ++t) {
+                if (static_cast<uint64_t>(pub.key[t]) < hi_u) continue;
+                const int64_t unit = static_cast<int64_t>(pub.phys[t]) * a.hkv + kvh;
                 prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.k_cache) + unit * kv_row, kv_row);
                 prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.v_cache) + unit * kv_row, kv_row);
             }
         }
-        pub.phys[t] = phys;
+    } else {
+        npub = ordered_keep(keys, nloc, lo_u - 1u, 0, sh, [&](int i, int pos) {
+            if (pos < kCandCap) {   // always: the count was checked; the guard bounds a logic error
+                pub.key[pos] = keys[i];
+                pub.logical[pos] = j0 + i;
+            }
+        });
+        __syncthreads();
+#pragma unroll 1
+        for (int t = tid; t < min(npub, kCandCap); t += kThreads) pub.phys[t] = phys_of(pub.logical[t] - j0, pub.key[t]);
     }
-    if (tid == 0) sh.pub_n = npub;
+    if (tid == 0) {
+        sh.pub_n = npub;
+        sh.nbin = 0;
+    }
     cluster_sync_all();   // every CTA's list is complete and visible
-    if (tid < CL) sh.cnt_r[tid] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.pub_n, tid)));
-    __syncthreads();
-    int off[CL + 1];
-    off[0] = 0;
-#pragma unroll
-    for (int r = 0; r < CL; ++r) off[r + 1] = off[r] + sh.cnt_r[r];
-    const int N = min(off[CL], kCandCap);
-    // gather: element i of the ascending list, from the CTA whose range holds it
+    // gather, one round of remote loads: element e = r kSlot + k is CTA r's k-th candidate,
+    // read with CTA r's count, so ascending e is ascending page order; thread t holds
+    // e = t, t + kThreads, t + 2 kThreads. A CTA with more than kSlot candidates (rare)
+    // makes every CTA gather again by offsets.
+    constexpr int kSlot = kCandCap / CL;
+    static_assert(kSlot * CL == 3 * kThreads, "three gathered elements per thread");
     uint32_t ck[3];
-    int cl[3], cp[3], eqf[3];
+    int cl[3], cp[3];
+    bool cv[3], over = false;
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
-        const int i = 3 * tid + u;
-        ck[u] = 0u;
-        cl[u] = cp[u] = 0;
-        if (i < N) {
-            int r = 0, first = 0;
-#pragma unroll
-            for (int q = 1; q < CL; ++q)
-                if (i >= off[q]) {
-                    r = q;
-                    first = off[q];
-                }
-            const int k = i - first;
-            ck[u] = ld_dsmem_u32(dsmem_addr(&pub.key[k], static_cast<uint32_t>(r)));
-            cl[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.logical[k], static_cast<uint32_t>(r))));
-            cp[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.phys[k], static_cast<uint32_t>(r))));
-        }
+        const int e = tid + u * kThreads, r = e / kSlot, k = e - r * kSlot;
+        const int cnt = static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.pub_n, static_cast<uint32_t>(r))));
+        ck[u] = ld_dsmem_u32(dsmem_addr(&pub.key[k], static_cast<uint32_t>(r)));
+        cl[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.logical[k], static_cast<uint32_t>(r))));
+        cp[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.phys[k], static_cast<uint32_t>(r))));
+        cv[u] = k < cnt;
+        over |= k == 0 && cnt > kSlot;
     }
     // the bin's keys, unordered, for the ranking
-    if (tid == 0) sh.nbin = 0;
-    __syncthreads();
+    auto bin_keys = [&]() {
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-        const bool m = 3 * tid + u < N && static_cast<uint64_t>(ck[u]) < hi_u;
-        const unsigned bal = __ballot_sync(0xffffffffu, m);
-        int bpos = 0;
-        if (lane == 0 && bal) bpos = atomicAdd(&sh.nbin, __popc(bal));
-        bpos = __shfl_sync(0xffffffffu, bpos, 0);
-        if (m) sh.rank_keys[bpos + __popc(bal & lanemask_lt())] = ck[u];
+        for (int u = 0; u < 3; ++u) {
+            const bool m = cv[u] && static_cast<uint64_t>(ck[u]) < hi_u;
+            const unsigned bal = __ballot_sync(0xffffffffu, m);
+            int bpos = 0;
+            if (lane == 0 && bal) bpos = atomicAdd(&sh.nbin, __popc(bal));
+            bpos = __shfl_sync(0xffffffffu, bpos, 0);
+            const int at = bpos + __popc(bal & lanemask_lt());
+            if (m && at < kRankCap) sh.rank_keys[at] = ck[u];   // always: the bin count was checked
+        }
+    };
+    bin_keys();
+    if (__syncthreads_or(over)) {
+        gather_by_offsets<CL>(pub, sh, ck, cl, cp, cv);
+        if (tid == 0) sh.nbin = 0;
+        __syncthreads();
+        bin_keys();
+        __syncthreads();
     }
-    __syncthreads();
     const int nb = min(sh.nbin, kRankCap);
     if (tid < nb) {
         const uint32_t key = sh.rank_keys[tid];
@@ -1119,31 +1310,39 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
         if (gt < remaining && ge >= remaining) {   // key is the remaining-th largest of the bin
             sh.rank_T = key;
             sh.rank_take = remaining - gt;
+            sh.rank_eq = ge - gt;
         }
     }
     __syncthreads();
     const uint32_t T = sh.rank_T;
     const int take = sh.rank_take;
-    // kept: every key > T, and the first `take` keys == T in page order
+    // kept: every key > T, and the first `take` keys == T in page order (all of them when
+    // T is not tied beyond `take`)
+    bool kp[3];
+    int pos[3];
+    if (take == sh.rank_eq) {
 #pragma unroll
-    for (int u = 0; u < 3; ++u) eqf[u] = (3 * tid + u < N && ck[u] == T) ? 1 : 0;
-    block_scan3(eqf, sh);
-    int kf[3];
+        for (int u = 0; u < 3; ++u) kp[u] = cv[u] && ck[u] >= T;
+    } else {
+        bool eqf[3];
 #pragma unroll
-    for (int u = 0; u < 3; ++u) kf[u] = (3 * tid + u < N && (ck[u] > T || (ck[u] == T && eqf[u] < take))) ? 1 : 0;
-    block_scan3(kf, sh);   // kf -> output positions
+        for (int u = 0; u < 3; ++u) eqf[u] = cv[u] && ck[u] == T;
+        scan_strided(eqf, pos, sh);
+        __syncthreads();   // the scan's totals read by every thread
+#pragma unroll
+        for (int u = 0; u < 3; ++u) kp[u] = cv[u] && (ck[u] > T || (eqf[u] && pos[u] < take));
+    }
+    scan_strided(kp, pos, sh);
     // the kept list (ascending) into the gathered-list arrays; this CTA writes its share of
     // selected[]
     const int share = (K + CL - 1) / CL;
     const int s0 = static_cast<int>(rank) * share, s1 = min(K, s0 + share);
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
-        const int i = 3 * tid + u;
-        const bool keep = i < N && (ck[u] > T || (ck[u] == T && eqf[u] < take));
-        if (keep && kf[u] < kCandCap) {
-            cand.logical[kf[u]] = cl[u];
-            cand.phys[kf[u]] = cp[u];
-            if (kf[u] >= s0 && kf[u] < s1) out[kf[u]] = cl[u];
+        if (kp[u] && pos[u] < kCandCap) {
+            cand.logical[pos[u]] = cl[u];
+            cand.phys[pos[u]] = cp[u];
+            if (pos[u] >= s0 && pos[u] < s1) out[pos[u]] = cl[u];
         }
     }
     *listed = true;
@@ -1196,25 +1395,29 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
     for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;   // rows gid, gid + 8
 
-    uint8_t* slot = ring + warp * kPageSlotBytes;
-    uint64_t* bar = &sh.bar[warp];
-    uint32_t phase = 0;
-    for (int p = p0 + warp; p < p1; p += kWarps) {
-        // tokens of the page that are attended
-        const int valid = p < n_sel ? kPage : min(kPage, tail - (p - n_sel) * kPage);
-        const bool listed = list_log && p < n_sel;
-        int logical = p < n_sel ? (listed ? list_log[p] : (sel_coherent ? __ldcg(sel + p) : sel[p]))
-                                : tail_page + (p - n_sel);
-        if (logical < 0 || logical >= a.max_pages) {
-            bad = true;
-            logical = 0;
+    // warp w attends pages p0 + w, p0 + w + kWarps, ...; page k of the warp goes to slot
+    // k mod kSlots, refilled with page k + kSlots once page k is attended
+    constexpr int kSlots = slots_per_warp(CL);
+    auto issue = [&](int p, int sl) {
+        int logical, phys;
+        if (list_log && p < n_sel) {   // the fused launch's kept list (shared memory)
+            logical = list_log[p];
+            phys = list_phys[p];
+        } else {
+            logical = p < n_sel ? (sel_coherent ? __ldcg(sel + p) : sel[p]) : tail_page + (p - n_sel);
+            if (logical < 0 || logical >= a.max_pages) {
+                bad = true;
+                logical = 0;
+            }
+            phys = a.page_table[static_cast<int64_t>(b) * a.max_pages + logical];
         }
-        int64_t phys = listed ? list_phys[p] : a.page_table[static_cast<int64_t>(b) * a.max_pages + logical];
         if (phys < 0 || phys >= a.num_phys) {
             bad = true;
             phys = 0;
         }
-        const int y = static_cast<int>((phys * a.hkv + kvh) * kPage);   // first row of the page's tile
+        const int y = static_cast<int>((static_cast<int64_t>(phys) * a.hkv + kvh) * kPage);   // the tile's first row
+        uint8_t* slot = ring + (sl * kWarps + warp) * kPageSlotBytes;
+        uint64_t* bar = &sh.bar[sl * kWarps + warp];
         fence_proxy_async_smem();   // earlier generic reads of the slot before the async refill
         __syncwarp();
         if (lane == 0) {
@@ -1224,8 +1427,18 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             tma_load_2d(slot + 2 * kBoxBytes, &a.tm_v, 0, y, bar);
             tma_load_2d(slot + 3 * kBoxBytes, &a.tm_v, 64, y, bar);
         }
-        if (!mbar_wait_bounded(bar, phase, a.st.wait_limit_ns)) failed = true;
-        phase ^= 1u;
+    };
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k)
+        if (p0 + warp + k * kWarps < p1) issue(p0 + warp + k * kWarps, k);
+    uint32_t phases = 0u;   // bit sl: the parity slot sl waits for next
+    int sl = 0;
+    for (int p = p0 + warp; p < p1; p += kWarps) {
+        // tokens of the page that are attended
+        const int valid = p < n_sel ? kPage : min(kPage, tail - (p - n_sel) * kPage);
+        const uint8_t* slot = ring + (sl * kWarps + warp) * kPageSlotBytes;
+        if (!mbar_wait_bounded(&sh.bar[sl * kWarps + warp], (phases >> sl) & 1u, a.st.wait_limit_ns)) failed = true;
+        phases ^= 1u << sl;
         const uint8_t* kslot = slot;
         const uint8_t* vslot = slot + 2 * kBoxBytes;
 
@@ -1304,6 +1517,8 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             mma_bf16_16816(o[nd + 1], pa, vb[2], vb[3]);
         }
         __syncwarp();   // all lanes done reading the slot before it is refilled
+        if (p + kSlots * kWarps < p1) issue(p + kSlots * kWarps, sl);
+        sl = kSlots == 1 ? 0 : sl ^ 1;
     }
     if (failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
     if (bad) report_error(a.st, LOCKS_ERR_BAD_INDEX);
@@ -1456,11 +1671,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     // a dependent kernel (the next layer's scorer) may be scheduled once every CTA
     // of this grid has started; it waits for this grid's completion itself
     allow_dependent_launch();
-    if (threadIdx.x < kWarps) mbar_init(&sh.bar[threadIdx.x], 1);
-    if (threadIdx.x == kWarps) mbar_init(&sh.sbar, 1);
+    if (threadIdx.x < 2 * kWarps) mbar_init(&sh.bar[threadIdx.x], 1);
+    if (threadIdx.x == 2 * kWarps) mbar_init(&sh.sbar, 1);
     if constexpr (MODE != SAMode::kAttend) {
         // the selection's per-warp key histograms (in the candidate-list space)
-        uint32_t* whist = reinterpret_cast<uint32_t*>(big + region_a_bytes(chunk));
+        uint32_t* whist = reinterpret_cast<uint32_t*>(big + region_a_bytes(chunk, CL));
         static_assert(kWarps * 256 * 4 <= kCandListBytes, "per-warp histograms fit a candidate list");
 #pragma unroll 1
         for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) whist[i] = 0u;
@@ -1488,7 +1703,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
             cluster_sync_all();
         }
         // fast selection: every CTA holds the kept pages, ascending, in its gathered list
-        const CandList kept = cand_list(big + region_a_bytes(chunk) + kCandListBytes);
+        const CandList kept = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
         attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, true,
                              true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr);
     }
@@ -1613,24 +1828,48 @@ int active_clusters_cl(size_t smem, SAMode mode) {
 
 size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode) {
     const size_t small = sizeof(SmallShared) + 1024;   // + alignment of the region after it
-    if (mode == SAMode::kAttend) return small + static_cast<size_t>(kRingBytes);
-    return small + static_cast<size_t>(region_a_bytes(chunk_of(max_pages, cluster))) + 2 * kCandListBytes;
+    const size_t need =
+        mode == SAMode::kAttend
+            ? small + static_cast<size_t>(ring_bytes(cluster))
+            : small + static_cast<size_t>(region_a_bytes(chunk_of(max_pages, cluster), cluster)) + 2 * kCandListBytes;
+    return cluster == kSpreadCluster ? std::max<size_t>(need, kSpreadSmemBytes) : need;
 }
 
 int group_bound(int g) { return g <= 4 ? 4 : 16; }
 
+namespace {
+template <int GM>
+int active_clusters_g(size_t smem, SAMode mode, int cluster) {
+    if (cluster == kSpreadCluster) return active_clusters_cl<kSpreadCluster, GM>(smem, mode);
+    return cluster == 16 ? active_clusters_cl<16, GM>(smem, mode) : active_clusters_cl<8, GM>(smem, mode);
+}
+template <int GM>
+cudaError_t launch_g(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream) {
+    if (cluster == kSpreadCluster) return launch_cl<kSpreadCluster, GM>(a, mode, stream);
+    return cluster == 16 ? launch_cl<16, GM>(a, mode, stream) : launch_cl<8, GM>(a, mode, stream);
+}
+}  // namespace
+
 int select_attend_active_clusters(int max_pages, SAMode mode, int g, int cluster) {
     const size_t smem = select_attend_smem_bytes(max_pages, cluster, mode);
-    if (group_bound(g) == 4)
-        return cluster == 16 ? active_clusters_cl<16, 4>(smem, mode) : active_clusters_cl<8, 4>(smem, mode);
-    return cluster == 16 ? active_clusters_cl<16, 16>(smem, mode) : active_clusters_cl<8, 16>(smem, mode);
+    return group_bound(g) == 4 ? active_clusters_g<4>(smem, mode, cluster) : active_clusters_g<16>(smem, mode, cluster);
+}
+
+int select_attend_ctas_per_sm(int max_pages, SAMode mode, int cluster) {
+    int dev = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    const size_t per_cta = select_attend_smem_bytes(max_pages, cluster, mode) + 1024;   // + the per-CTA reserve
+    return std::max(1, std::min(2, static_cast<int>(static_cast<size_t>(per_sm) / per_cta)));
 }
 
 cudaError_t launch_select_attend(const SelectAttendArgs& a, SAMode mode, int cluster, cudaStream_t stream) {
     if (a.batch * a.hkv == 0) return cudaSuccess;
     const int g = a.hq / a.hkv;
-    if (group_bound(g) == 4) return cluster == 16 ? launch_cl<16, 4>(a, mode, stream) : launch_cl<8, 4>(a, mode, stream);
-    return cluster == 16 ? launch_cl<16, 16>(a, mode, stream) : launch_cl<8, 16>(a, mode, stream);
+    return group_bound(g) == 4 ? launch_g<4>(a, mode, cluster, stream) : launch_g<16>(a, mode, cluster, stream);
 }
 
 }  // namespace locks

@@ -105,6 +105,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
             "locks_get_device_status": ([P, ctypes.POINTER(I32), P], ctypes.c_int),
             "locks_clear_device_status": ([P, P], ctypes.c_int),
             "locks_set_wait_limit_ns": ([U64], ctypes.c_int),
+            "locks_set_select_cluster": ([ctypes.c_int32], ctypes.c_int),
             "locks_selftest_bounded_wait": ([P, S, U64, P], ctypes.c_int),
             "locks_ablation_workspace_size": ([D, ctypes.POINTER(S)], ctypes.c_int),
             "locks_exact_scores": ([D, P, P, P, P, P, P, S, P], ctypes.c_int),
@@ -307,6 +308,11 @@ def locks_clear_device_status(workspace, stream=None) -> None:
 
 def locks_set_wait_limit_ns(ns: int) -> None:
     _check("locks_set_wait_limit_ns", load_library().locks_set_wait_limit_ns(int(ns)))
+
+
+def locks_set_select_cluster(cluster: int) -> None:
+    """Pins the cluster size (8, 12 or 16 CTAs) of launches that select pages; 0 = automatic."""
+    _check("locks_set_select_cluster", load_library().locks_set_select_cluster(int(cluster)))
 
 
 def locks_selftest_bounded_wait(workspace, limit_ns: int, stream=None) -> None:

@@ -85,6 +85,10 @@ def test_host_validation_codes(lib):
     assert so.locks_score_pages(ctypes.byref(empty), None, S, None, None, None, None, None, 0, None) == L.LOCKS_OK
     assert so.locks_build_summaries(ctypes.byref(ok), None, None, 0, S, None, 0, None) == L.LOCKS_OK
     assert so.locks_build_summaries(ctypes.byref(ok), None, None, -1, S, None, 0, None) == L.LOCKS_ERR_INVALID_ARG
+    for cl in (1, 4, 10, 32, -8):            # only 0 (automatic), 8, 12 and 16 are accepted
+        assert so.locks_set_select_cluster(cl) == L.LOCKS_ERR_INVALID_ARG
+    for cl in (8, 12, 16, 0):
+        assert so.locks_set_select_cluster(cl) == L.LOCKS_OK
 
 
 def test_noalloc_rejects_oversized_problems_on_the_host(lib):

@@ -334,6 +334,44 @@ def _attend_on(prob, k_cap, selected, n_selected):
                                                       ("batch8_256k", 400, 3, 512), ("glm9b_4x1m", 600, 2, 512),
                                                       ("ctx1m", 900, 1, 2048)])
 def test_decode_step_matches_oracle(wname, pages, batch, budget):
+    _check_decode_step(wname, pages, batch, budget)
+
+
+@pytest.fixture
+def pin_cluster():
+    """Pins the selection launches' cluster size for one test, restoring the automatic
+    choice afterwards."""
+    def pin(cl):
+        L.locks_set_select_cluster(cl)
+    yield pin
+    L.locks_set_select_cluster(0)
+
+
+@pytest.mark.parametrize("cluster", [8, 12, 16])
+@pytest.mark.parametrize("g,hkv,budget", [(4, 8, 160), (16, 2, 2048), (1, 1, 16), (3, 2, 100000)])
+def test_selection_parity_every_cluster_size(pin_cluster, cluster, g, hkv, budget):
+    """Each cluster size the launcher may pick (12 CTAs: one per SM) selects the oracle's
+    pages, on ragged sequences with a block of exact ties."""
+    pin_cluster(cluster)
+    rng = np.random.default_rng(7 * cluster + g + budget)
+    B, maxp = 3, 2500
+    scores = rng.standard_normal((B, hkv * g, maxp)) * 2.0
+    scores[0, :, 700:760] = 0.5
+    seq = np.array([2500, 1201, 11], np.int32)
+    sel, n, keys, osel, on, okeys = _select_case(scores, seq, budget, hkv)
+    check_selection(sel, n, osel, on, okeys, seq)
+    for b in range(B):
+        assert np.abs(keys[b, :, :seq[b]] - okeys[b, :, :seq[b]]).max() < 1e-5
+
+
+@pytest.mark.parametrize("cluster", [8, 12, 16])
+@pytest.mark.parametrize("wname,pages,batch,budget", [("ctx1m", 900, 1, 2048), ("glm9b_4x1m", 600, 2, 512)])
+def test_decode_step_every_cluster_size(pin_cluster, cluster, wname, pages, batch, budget):
+    pin_cluster(cluster)
+    _check_decode_step(wname, pages, batch, budget)
+
+
+def _check_decode_step(wname, pages, batch, budget):
     w = synth.WORKLOADS[wname]
     if pages is not None:
         w = w.scaled(pages=pages, batch=batch)
