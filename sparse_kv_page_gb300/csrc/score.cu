@@ -71,10 +71,6 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
     uint64_t* empty = full + kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // The grid is persistent (at most one CTA per SM), so a dependent kernel (the
-    // selection) only takes SMs this kernel has left; it may be scheduled as soon
-    // as they free up (the trigger completes once every CTA has started).
-    allow_dependent_launch();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 33);              // 1 expect_tx arrive + 32 LDGSTS arrives
@@ -85,6 +81,11 @@ __global__ void __launch_bounds__(Shape<NT>::kThreads, 1) score_kernel(ScoreArgs
     // launched with programmatic stream serialization: the set-up above overlaps
     // the end of the previous kernel; every global access follows
     grid_dependency_wait();
+    // The grid is persistent (at most one CTA per SM), so a dependent kernel (the
+    // selection) only takes SMs this kernel has left; it may be scheduled as soon
+    // as they free up. The trigger follows the wait, so a dependent that reads
+    // inputs before its own wait sees everything the kernels before this one wrote.
+    allow_dependent_launch();
     __syncthreads();
 
     const int per = (total_items + gridDim.x - 1) / gridDim.x;

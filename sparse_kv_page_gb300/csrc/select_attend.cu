@@ -1057,9 +1057,10 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     const CandList cand = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
     *listed = false;
     const int g = a.hq / a.hkv;
-    // Loads that do not depend on the sequence length go out first: this CTA's nominal page
-    // range [jn0, jn0 + nn) of the score rows (bulk copies into the staging buffer), an L2
-    // prefetch of its page-table entries, and the query rows.
+    // This CTA's nominal page range [jn0, jn0 + nn). Inputs go out before the wait for the
+    // scorer (an L2 prefetch of the range's page-table entries, the query rows, the
+    // sequence length), the range's score rows (bulk copies into the staging buffer)
+    // right after it.
     const int jn0 = min(a.max_pages, static_cast<int>(rank) * chunk);
     const int nn = min(chunk, a.max_pages - jn0);
     const int64_t stride = a.max_pages;
@@ -1068,13 +1069,16 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     // groups of more than four heads read their scores with loads (staging them four rows at
     // a time would serialise the copies)
     const bool staged = GM <= kHB && vec && nn > 0 && kHB * chunk * 4 <= stage_cap(CL);
-    if (tid == 0 && staged) stage_rows(srow, stride, 0, min(g, kHB), jn0, nn, chunk, reinterpret_cast<float*>(keys), sh);
     if (tid == 32 && nn > 0 && a.page_table && vec && (reinterpret_cast<uintptr_t>(a.page_table) & 15) == 0)
         prefetch_l2_bulk(a.page_table + static_cast<int64_t>(b) * a.max_pages + jn0,
                          static_cast<uint32_t>((nn + 3) & ~3) * 4u);
     float qv[16 * kD / kThreads];
     if (stage_q) load_query(a, b, kvh, g, qv);
     const int seq_len = a.seq_pages[b];
+    // the scores and partials come from the previous kernel (the scorer)
+    grid_dependency_wait();
+    allow_dependent_launch();   // the next kernel waits for this grid's completion itself
+    if (tid == 0 && staged) stage_rows(srow, stride, 0, min(g, kHB), jn0, nn, chunk, reinterpret_cast<float*>(keys), sh);
     bool failed = false;
     if (staged && !a.lse_partials && !mbar_wait_bounded(&sh.sbar, 0, a.st.wait_limit_ns)) failed = true;
 
@@ -1668,9 +1672,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     const uint32_t rank = cluster_ctarank();
     const int seg = blockIdx.y;
     const int b = seg / a.hkv, kvh = seg % a.hkv;
-    // a dependent kernel (the next layer's scorer) may be scheduled once every CTA
-    // of this grid has started; it waits for this grid's completion itself
-    allow_dependent_launch();
     if (threadIdx.x < 2 * kWarps) mbar_init(&sh.bar[threadIdx.x], 1);
     if (threadIdx.x == 2 * kWarps) mbar_init(&sh.sbar, 1);
     if constexpr (MODE != SAMode::kAttend) {
@@ -1681,9 +1682,15 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
         for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) whist[i] = 0u;
     }
     fence_barrier_init();
-    // launched with programmatic stream serialization: the set-up above overlaps
-    // the end of the previous kernel (the scorer); every global access follows
-    grid_dependency_wait();
+    // Launched with programmatic stream serialization: the set-up above overlaps the end
+    // of the previous kernel (the scorer). The selection waits for it inside select_pages,
+    // after loading inputs that kernel does not write (the query, sequence lengths and a
+    // prefetch of the page table): every kernel of this library lets its dependents
+    // launch only after its own wait, so the kernels before it are complete.
+    if constexpr (MODE == SAMode::kAttend) {
+        grid_dependency_wait();
+        allow_dependent_launch();   // the next kernel waits for this grid's completion itself
+    }
     __syncthreads();
 
     if constexpr (MODE == SAMode::kSelect) {
