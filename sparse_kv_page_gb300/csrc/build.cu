@@ -30,6 +30,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kKStride = 136;   // bf16 row stride of the keys in shared memory (conflict-free fragments)
 constexpr int kMaxSweeps = 10;
+constexpr int64_t kSingleUnitBuild = 512;   // builds of at most this many units: one unit per warp
 constexpr int kCtasPerSm = 3;   // 12 warps per SM at 168 registers (the shared memory allows it)
 
 // The keys stay in bf16 (exact) and D = K - mu is formed on the fly in fp32, which keeps
@@ -160,7 +161,12 @@ __device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, 
             *reinterpret_cast<uint4*>(k + (c >> 4) * kKStride + (c & 15) * 8) = v[m];
         }
     } else {
-        for (int idx = lane; idx < kPage * kD; idx += 32) k[(idx / kD) * kKStride + idx % kD] = 0;
+        // no unit: a zero Gram (its Jacobi ends at once; nothing of it is written out)
+        float* g = w.g[slot];
+        for (int idx = lane; idx < kPage * kPage; idx += 32) g[idx] = 0.f;
+        if (lane == 0) w.sig[slot][0] = __int_as_float(0);
+        __syncwarp();
+        return;
     }
     __syncwarp();
     // mean over the 16 keys, lane -> dims 4 lane .. 4 lane + 3
@@ -458,16 +464,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) build_kernel(BuildArgs a
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WarpSmem& w = reinterpret_cast<WarpSmem*>(smem)[warp];
     const int64_t n_units = static_cast<int64_t>(a.n_pages) * a.hkv;
-    const int64_t n_pairs = (n_units + 1) / 2;
+    // small builds (a page that just filled) take one unit per warp: its second
+    // half-warp's Jacobi is idle, but the unit's set-up and packing are not queued
+    // behind another unit's
+    const bool single = n_units <= kSingleUnitBuild;
+    const int64_t n_pairs = single ? n_units : (n_units + 1) / 2;
     for (int64_t pi = static_cast<int64_t>(blockIdx.x) * kWarps + warp; pi < n_pairs;
          pi += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const int64_t u0 = 2 * pi, u1 = (2 * pi + 1 < n_units) ? 2 * pi + 1 : -1;
+        const int64_t u0 = single ? pi : 2 * pi, u1 = (!single && 2 * pi + 1 < n_units) ? 2 * pi + 1 : -1;
         const int64_t v0 = valid_unit(a, u0), v1 = valid_unit(a, u1);
         load_centre_gram(a, v0, w, 0, lane);
         load_centre_gram(a, v1, w, 1, lane);
         jacobi_top8(w, lane);
         finish_unit(a, v0, w, 0, lane);
-        finish_unit(a, v1, w, 1, lane);
+        if (u1 >= 0) finish_unit(a, v1, w, 1, lane);
     }
 }
 
@@ -479,7 +489,7 @@ cudaError_t launch_build(const BuildArgs& a, int num_sms, cudaStream_t stream) {
     const size_t smem = kWarps * sizeof(WarpSmem);
     cudaError_t e = ensure_kernel_attrs<build_kernel>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t pairs = (n_units + 1) / 2;
+    const int64_t pairs = n_units <= kSingleUnitBuild ? n_units : (n_units + 1) / 2;
     int64_t grid = (pairs + kWarps - 1) / kWarps;
     const int64_t cap = static_cast<int64_t>(num_sms) * kCtasPerSm;
     if (grid > cap) grid = cap;

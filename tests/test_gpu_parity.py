@@ -490,10 +490,10 @@ def _key_pages(rng, n):
     return synth.f32_to_bf16_bits(np.stack(pages).astype(np.float32))
 
 
-@pytest.mark.parametrize("hkv", [1, 2, 8])
-def test_builder_invariants(hkv):
-    rng = np.random.default_rng(hkv)
-    nphys = 41
+@pytest.mark.parametrize("hkv,nphys", [(1, 41), (2, 41), (8, 41), (8, 90)])
+def test_builder_invariants(hkv, nphys):
+    """Up to 512 units the builder takes one unit per warp, above it two; both are covered."""
+    rng = np.random.default_rng(hkv + nphys)
     keys = _key_pages(rng, nphys * hkv).reshape(nphys, hkv, 16, 128)
     ids = np.array([p for p in range(nphys) if p % 4 != 1], np.int32)   # some pages not listed
     dims = L.make_dims(1, hkv, hkv, nphys, nphys)
