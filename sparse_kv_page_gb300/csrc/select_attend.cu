@@ -451,20 +451,57 @@ __device__ __forceinline__ void warp_span(int n, int w, int& w0, int& w1) {
     w1 = min(n, w0 + per);
 }
 
-// The group keys of this CTA's pages [j0, j1) into keys[] (order-preserving uint32 images)
-// and, when hist0, the fast first radix pass's histogram of them into sh.hist[0] (zeroed
-// by the caller), from sh.Lh. In the log2 domain x_h = s_h log2 e - L_h log2 e <= 0 and
-// key = log2(sum_h 2^x_h) ln 2 - ln g; each term is at most 1, so the sum needs no shift
-// unless it underflows (every share below 2^-100), when the page is redone with its
-// largest term factored out. A NaN score makes its page's key NaN (ranked last).
-// Staged scores (see select_pages) are read from shared memory, a batch of four heads at
-// a time (groups of more than four heads re-stage the next batch after each); keys[]
-// overlays the first staged row, each thread reading a slab's scores before writing its
-// keys. Otherwise the scores are read from global memory.
+// Pages whose unshifted sum underflowed in the staged key loop (every share below 2^-100,
+// or none): the key again with the largest term factored out, from the scores in global
+// memory (staged row 0 now holds the keys); the histogram is corrected. Out of line: rare.
+__device__ __noinline__ void keys_underflow_fixup(const float* srow, int64_t stride, int g, int j0, int w0, int w1,
+                                                  uint32_t* keys, float4 Lp4, float log_g, bool hist0,
+                                                  const RadixRange fr, uint32_t* whist) {
+    const float Lp[kHB] = {Lp4.x, Lp4.y, Lp4.z, Lp4.w};
+#pragma unroll 1
+    for (int jj = w0 + 4 * (threadIdx.x & 31); jj < w1; jj += 128) {
+#pragma unroll 1
+        for (int e = 0; e < 4 && jj + e < w1; ++e) {
+            float x[kHB], m = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < kHB; ++hh) {
+                x[hh] = hh < g ? fmaf(no_nan(__ldcg(srow + hh * stride + j0 + jj + e)), kLog2e, -Lp[hh]) : -INFINITY;
+                m = fmaxf(m, x[hh]);
+            }
+            float z = 0.f, zz = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < kHB; ++hh) {
+                z += fast_exp2(x[hh]);
+                zz += fast_exp2(x[hh] - m);
+            }
+            const uint32_t old_u = keys[jj + e];
+            if (old_u == 0u || z >= 7.9e-31f) continue;   // NaN key, or no underflow
+            const float key2 = m == -INFINITY ? -INFINITY : m + fast_log2(zz);
+            const uint32_t u = orderable_key(key2 * kLn2 - log_g);
+            if (hist0) {
+                const uint32_t d0 = fast_digit(old_u, fr), d1 = fast_digit(u, fr);
+                if (d0 != 0u) atomicSub(&whist[(threadIdx.x >> 5) * 256 + d0], 1u);
+                if (d1 != 0u) atomicAdd(&whist[(threadIdx.x >> 5) * 256 + d1], 1u);
+            }
+            keys[jj + e] = u;
+        }
+    }
+}
+// The optional key output (tests), once every thread's keys are final. Out of line.
+__device__ __noinline__ void keys_out(float* kout, const uint32_t* keys, int nloc) {
+    __syncthreads();
+#pragma unroll 1
+    for (int i = threadIdx.x; i < nloc; i += kThreads) kout[i] = key_of_image(keys[i]);
+}
+
+// group_keys for scores read with loads (rows not staged) or groups of more than four
+// heads (staged four rows at a time). Returns whether a staging wait timed out. Called
+// inline for large groups (their normal path) and out of line otherwise (rare), so that
+// the staged path's code is contiguous.
 template <int GM>
-__device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, int chunk, uint32_t* keys,
-                           SmallShared& sh, bool staged, const RadixRange& fr, bool hist0, uint32_t* whist,
-                           bool& failed) {
+__device__ __forceinline__ bool group_keys_loads(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, int chunk, uint32_t* keys,
+                           SmallShared& sh, bool staged, const RadixRange fr, bool hist0, uint32_t* whist) {
+    bool failed = false;
     const int tid = threadIdx.x;
     const int g = a.hq / a.hkv;
     const int nloc = j1 - j0;
@@ -489,78 +526,7 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
         }
         return u;
     };
-    if (GM <= kHB && staged) {
-        // staged rows: warp w takes the pages of warp_span, lane l the slabs of 4 pages at
-        // 4 l, 4 l + 128, ... of them (so warp w's histogram counts exactly that range);
-        // shared memory by window address, the histogram by shared reductions; the rare
-        // underflow and the optional key output are handled after the loop
-        const uint32_t s_base = smem_u32(stg);
-        const uint32_t wh = smem_u32(whist) + static_cast<uint32_t>(threadIdx.x >> 5) * 1024u;
-        int w0, w1;
-        warp_span(nloc, threadIdx.x >> 5, w0, w1);
-        bool uf = false;
-#pragma unroll 1
-        for (int jj = w0 + 4 * (tid & 31); jj < w1; jj += 128) {
-            float4 v[kHB];
-#pragma unroll
-            for (int hh = 0; hh < kHB; ++hh) {
-                // rows past the group are not staged: read (inside the region) and ignored
-                v[hh] = lds_f4(s_base + static_cast<uint32_t>(hh * chunk + jj) * 4u);
-                if (hh >= g) v[hh] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
-            uint32_t k4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float z = 0.f;
-#pragma unroll
-                for (int hh = 0; hh < kHB; ++hh) z += fast_exp2(fmaf(comp(v[hh], e), kLog2e, -Lp[hh]));
-                uf |= !(z >= 7.9e-31f) && z == z;   // every share below 2^-100 (or none): redone below
-                const uint32_t u = orderable_key(fast_log2(z) * kLn2 - log_g);
-                const uint32_t d = fast_digit(u, fr);
-                red_shared_add_if(hist0 && d != 0u && jj + e < w1, wh + d * 4u, 1u);
-                k4[e] = u;
-            }
-            sts_u4(s_base + static_cast<uint32_t>(jj) * 4u, make_uint4(k4[0], k4[1], k4[2], k4[3]));
-        }
-        if (__syncthreads_or(uf)) {
-            // pages whose sum underflowed: the key again with the largest term factored out,
-            // from the scores in global memory (row 0 is overwritten by the keys)
-#pragma unroll 1
-            for (int jj = w0 + 4 * (tid & 31); jj < w1; jj += 128) {
-#pragma unroll 1
-                for (int e = 0; e < 4 && jj + e < w1; ++e) {
-                    float x[kHB], m = -INFINITY;
-#pragma unroll
-                    for (int hh = 0; hh < kHB; ++hh) {
-                        x[hh] = hh < g ? fmaf(no_nan(__ldcg(srow + hh * stride + j0 + jj + e)), kLog2e, -Lp[hh])
-                                       : -INFINITY;
-                        m = fmaxf(m, x[hh]);
-                    }
-                    float z = 0.f, zz = 0.f;
-#pragma unroll
-                    for (int hh = 0; hh < kHB; ++hh) {
-                        z += fast_exp2(x[hh]);
-                        zz += fast_exp2(x[hh] - m);
-                    }
-                    const uint32_t old_u = keys[jj + e];
-                    if (old_u == 0u || z >= 7.9e-31f) continue;   // NaN key, or no underflow
-                    const float key2 = m == -INFINITY ? -INFINITY : m + fast_log2(zz);
-                    const uint32_t u = orderable_key(key2 * kLn2 - log_g);
-                    if (hist0) {
-                        const uint32_t d0 = fast_digit(old_u, fr), d1 = fast_digit(u, fr);
-                        if (d0 != 0u) atomicSub(&whist[(threadIdx.x >> 5) * 256 + d0], 1u);
-                        if (d1 != 0u) atomicAdd(&whist[(threadIdx.x >> 5) * 256 + d1], 1u);
-                    }
-                    keys[jj + e] = u;
-                }
-            }
-        }
-        if (kout) {
-            __syncthreads();   // every thread's keys final
-#pragma unroll 1
-            for (int i = tid; i < nloc; i += kThreads) kout[j0 + i] = key_of_image(keys[i]);
-        }
-    } else if constexpr (GM <= kHB) {
+    if constexpr (GM <= kHB) {
         // a rolled loop over this thread's slabs (instruction fetch is part of this code's
         // latency: it runs about once per launch), the slab's four pages in parallel
 #pragma unroll 1
@@ -666,6 +632,84 @@ __device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, in
                 *reinterpret_cast<uint4*>(keys + (j - j0)) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
             }
         }
+    }
+    return failed;
+}
+template <int GM>
+__device__ __noinline__ bool group_keys_loads_ool(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, int chunk,
+                                                  uint32_t* keys, SmallShared& sh, bool staged, const RadixRange fr,
+                                                  bool hist0, uint32_t* whist) {
+    return group_keys_loads<GM>(a, b, kvh, j0, j1, chunk, keys, sh, staged, fr, hist0, whist);
+}
+
+// The group keys of this CTA's pages [j0, j1) into keys[] (order-preserving uint32 images)
+// and, when hist0, the fast first radix pass's histogram of them into sh.hist[0] (zeroed
+// by the caller), from sh.Lh. In the log2 domain x_h = s_h log2 e - L_h log2 e <= 0 and
+// key = log2(sum_h 2^x_h) ln 2 - ln g; each term is at most 1, so the sum needs no shift
+// unless it underflows (every share below 2^-100), when the page is redone with its
+// largest term factored out. A NaN score makes its page's key NaN (ranked last).
+// Staged scores (see select_pages) are read from shared memory, a batch of four heads at
+// a time (groups of more than four heads re-stage the next batch after each); keys[]
+// overlays the first staged row, each thread reading a slab's scores before writing its
+// keys. Otherwise the scores are read from global memory.
+template <int GM>
+__device__ void group_keys(const SelectAttendArgs& a, int b, int kvh, int j0, int j1, int chunk, uint32_t* keys,
+                           SmallShared& sh, bool staged, const RadixRange& fr, bool hist0, uint32_t* whist,
+                           bool& failed) {
+    const int tid = threadIdx.x;
+    const int g = a.hq / a.hkv;
+    const int nloc = j1 - j0;
+    const int64_t stride = a.max_pages;
+    const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * stride;
+    const float* stg = reinterpret_cast<const float*>(keys);
+    const float log_g = logf(static_cast<float>(g));
+    float Lp[GM];
+#pragma unroll
+    for (int hh = 0; hh < GM; ++hh) Lp[hh] = hh < g ? sh.Lh[hh] * kLog2e : 0.f;
+    float* kout = a.sel_keys ? a.sel_keys + (static_cast<int64_t>(b) * a.hkv + kvh) * a.max_pages : nullptr;
+    if (GM <= kHB && staged) {
+        // staged rows: warp w takes the pages of warp_span, lane l the slabs of 4 pages at
+        // 4 l, 4 l + 128, ... of them (so warp w's histogram counts exactly that range);
+        // shared memory by window address, the histogram by shared reductions; the rare
+        // underflow and the optional key output are handled after the loop
+        const uint32_t s_base = smem_u32(stg);
+        const uint32_t wh = smem_u32(whist) + static_cast<uint32_t>(threadIdx.x >> 5) * 1024u;
+        int w0, w1;
+        warp_span(nloc, threadIdx.x >> 5, w0, w1);
+        bool uf = false;
+#pragma unroll 1
+        for (int jj = w0 + 4 * (tid & 31); jj < w1; jj += 128) {
+            float4 v[kHB];
+#pragma unroll
+            for (int hh = 0; hh < kHB; ++hh) {
+                // rows past the group are not staged: read (inside the region) and ignored
+                v[hh] = lds_f4(s_base + static_cast<uint32_t>(hh * chunk + jj) * 4u);
+                if (hh >= g) v[hh] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            uint32_t k4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float z = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < kHB; ++hh) z += fast_exp2(fmaf(comp(v[hh], e), kLog2e, -Lp[hh]));
+                uf |= !(z >= 7.9e-31f) && z == z;   // every share below 2^-100 (or none): redone below
+                const uint32_t u = orderable_key(fast_log2(z) * kLn2 - log_g);
+                const uint32_t d = fast_digit(u, fr);
+                red_shared_add_if(hist0 && d != 0u && jj + e < w1, wh + d * 4u, 1u);
+                k4[e] = u;
+            }
+            sts_u4(s_base + static_cast<uint32_t>(jj) * 4u, make_uint4(k4[0], k4[1], k4[2], k4[3]));
+        }
+        if (__syncthreads_or(uf))
+            keys_underflow_fixup(srow, stride, g, j0, w0, w1, keys,
+                                 make_float4(Lp[0], GM > 1 ? Lp[1 % GM] : 0.f, GM > 2 ? Lp[2 % GM] : 0.f,
+                                             GM > 3 ? Lp[3 % GM] : 0.f),
+                                 log_g, hist0, fr, whist);
+        if (kout) keys_out(kout + j0, keys, nloc);
+    } else if constexpr (GM > kHB) {   // the normal path of large groups: inline
+        failed |= group_keys_loads<GM>(a, b, kvh, j0, j1, chunk, keys, sh, staged, fr, hist0, whist);
+    } else {                           // unstaged rows: rare, out of line
+        failed |= group_keys_loads_ool<GM>(a, b, kvh, j0, j1, chunk, keys, sh, staged, fr, hist0, whist);
     }
     __syncthreads();
     if (hist0) {
@@ -796,35 +840,73 @@ __device__ __forceinline__ CandList cand_list(uint8_t* base) {
 }
 
 // The gather when some CTA published more than its fixed share of slots: element e of the
-// ascending list comes from the CTA whose offset range holds it (the counts read first).
-// Same layout as the fixed-slot gather.
+// ascending list comes from the CTA whose offset range holds it (the counts read first),
+// written to `to` (this CTA's gathered-list arrays) at index e. Returns the list length.
+// Out of line: rare.
 template <int CL>
-__device__ __forceinline__ void gather_by_offsets(const CandList& pub, SmallShared& sh, uint32_t (&ck)[3],
-                                               int (&cl)[3], int (&cp)[3], bool (&cv)[3]) {
-    const int tid = threadIdx.x;
+__device__ __noinline__ int gather_by_offsets(const CandList pub, const CandList to, SmallShared& sh) {
     int off[CL + 1];
     off[0] = 0;
 #pragma unroll
     for (int r = 0; r < CL; ++r)
         off[r + 1] = off[r] + static_cast<int>(ld_dsmem_u32(dsmem_addr(&sh.pub_n, static_cast<uint32_t>(r))));
     const int N = min(off[CL], kCandCap);
+#pragma unroll 1
+    for (int e = threadIdx.x; e < N; e += kThreads) {
+        int r = 0, first = 0;
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-        const int e = tid + u * kThreads;
-        cv[u] = e < N;
-        if (cv[u]) {
-            int r = 0, first = 0;
-#pragma unroll
-            for (int q = 1; q < CL; ++q) {
-                r = e >= off[q] ? q : r;
-                first = e >= off[q] ? off[q] : first;
-            }
-            const int k = e - first;
-            ck[u] = ld_dsmem_u32(dsmem_addr(&pub.key[k], static_cast<uint32_t>(r)));
-            cl[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.logical[k], static_cast<uint32_t>(r))));
-            cp[u] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.phys[k], static_cast<uint32_t>(r))));
+        for (int q = 1; q < CL; ++q) {
+            r = e >= off[q] ? q : r;
+            first = e >= off[q] ? off[q] : first;
         }
+        const int k = e - first;
+        to.key[e] = ld_dsmem_u32(dsmem_addr(&pub.key[k], static_cast<uint32_t>(r)));
+        to.logical[e] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.logical[k], static_cast<uint32_t>(r))));
+        to.phys[e] = static_cast<int>(ld_dsmem_u32(dsmem_addr(&pub.phys[k], static_cast<uint32_t>(r))));
     }
+    return N;
+}
+
+// The candidates' publication when the keys were not computed by warp ranges (scores read
+// with loads, or groups of more than four heads): an ordered compaction of the keys >= lo_u,
+// then each candidate's physical page (the staged page-table entry, or global memory) and an
+// L2 prefetch of its K/V when it is kept for sure (key >= hi_u). Returns the count. Inline
+// for large groups (their normal path), out of line otherwise.
+__device__ __forceinline__ int publish_ordered(const SelectAttendArgs& a, int b, int kvh, int j0, int nloc,
+                                            const uint32_t* keys, uint32_t lo_u, uint64_t hi_u, const int32_t* ptab,
+                                            bool ptab_staged, bool paged, const CandList pub, SmallShared& sh) {
+    const int npub = ordered_keep(keys, nloc, lo_u - 1u, 0, sh, [&](int i, int pos) {
+        if (pos < kCandCap) {   // always: the count was checked; the guard bounds a logic error
+            pub.key[pos] = keys[i];
+            pub.logical[pos] = j0 + i;
+        }
+    });
+    __syncthreads();
+    const int64_t kv_row = static_cast<int64_t>(kPage) * kD * 2;   // bytes per (page, kv head)
+#pragma unroll 1
+    for (int t = threadIdx.x; t < min(npub, kCandCap); t += kThreads) {
+        int phys = 0;
+        if (paged) {
+            const int i = pub.logical[t] - j0;
+            phys = ptab_staged ? ptab[i] : a.page_table[static_cast<int64_t>(b) * a.max_pages + j0 + i];
+            if (phys < 0 || phys >= a.num_phys) {
+                report_error(a.st, LOCKS_ERR_BAD_INDEX);
+                phys = 0;
+            }
+            if (static_cast<uint64_t>(pub.key[t]) >= hi_u) {
+                const int64_t unit = static_cast<int64_t>(phys) * a.hkv + kvh;
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.k_cache) + unit * kv_row, kv_row);
+                prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.v_cache) + unit * kv_row, kv_row);
+            }
+        }
+        pub.phys[t] = phys;
+    }
+    return npub;
+}
+__device__ __noinline__ int publish_ordered_ool(const SelectAttendArgs& a, int b, int kvh, int j0, int nloc,
+                                                const uint32_t* keys, uint32_t lo_u, uint64_t hi_u, const int32_t* ptab,
+                                                bool ptab_staged, bool paged, const CandList pub, SmallShared& sh) {
+    return publish_ordered(a, b, kvh, j0, nloc, keys, lo_u, hi_u, ptab, ptab_staged, paged, pub, sh);
 }
 
 // One radix pass's cluster step: sums the CTAs' histograms `hist` (256 bins) through
@@ -1148,22 +1230,6 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     // no table or caches)
     bool pt_failed = ptab_staged && !mbar_wait_bounded(&sh.sbar, ptab_phase & 1u, a.st.wait_limit_ns);
     if (pt_failed) report_error(a.st, LOCKS_ERR_TIMEOUT);
-    // a candidate's physical page (the staged page-table entry, or global memory), with an
-    // L2 prefetch of its K/V when it is kept for sure
-    auto phys_of = [&](int i, uint32_t key) -> int {
-        if (!paged) return 0;
-        int phys = ptab_staged ? ptab[i] : a.page_table[static_cast<int64_t>(b) * a.max_pages + j0 + i];
-        if (phys < 0 || phys >= a.num_phys) {
-            report_error(a.st, LOCKS_ERR_BAD_INDEX);
-            phys = 0;
-        }
-        if (static_cast<uint64_t>(key) >= hi_u) {
-            const int64_t unit = static_cast<int64_t>(phys) * a.hkv + kvh;
-            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.k_cache) + unit * kv_row, kv_row);
-            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.v_cache) + unit * kv_row, kv_row);
-        }
-        return phys;
-    };
     int npub = 0;
     if (GM <= kHB && staged) {
         // warp w computed the keys of warp_span w, so its candidates are counted by its
@@ -1246,15 +1312,10 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
             }
         }
     } else {
-        npub = ordered_keep(keys, nloc, lo_u - 1u, 0, sh, [&](int i, int pos) {
-            if (pos < kCandCap) {   // always: the count was checked; the guard bounds a logic error
-                pub.key[pos] = keys[i];
-                pub.logical[pos] = j0 + i;
-            }
-        });
-        __syncthreads();
-#pragma unroll 1
-        for (int t = tid; t < min(npub, kCandCap); t += kThreads) pub.phys[t] = phys_of(pub.logical[t] - j0, pub.key[t]);
+        if constexpr (GM > kHB)   // the normal path of large groups: inline
+            npub = publish_ordered(a, b, kvh, j0, nloc, keys, lo_u, hi_u, ptab, ptab_staged, paged, pub, sh);
+        else
+            npub = publish_ordered_ool(a, b, kvh, j0, nloc, keys, lo_u, hi_u, ptab, ptab_staged, paged, pub, sh);
     }
     if (tid == 0) {
         sh.pub_n = npub;
@@ -1295,7 +1356,16 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     };
     bin_keys();
     if (__syncthreads_or(over)) {
-        gather_by_offsets<CL>(pub, sh, ck, cl, cp, cv);
+        const int N = gather_by_offsets<CL>(pub, cand, sh);
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int e = tid + u * kThreads;
+            cv[u] = e < N;
+            ck[u] = cv[u] ? cand.key[e] : 0u;
+            cl[u] = cv[u] ? cand.logical[e] : 0;
+            cp[u] = cv[u] ? cand.phys[e] : 0;
+        }
         if (tid == 0) sh.nbin = 0;
         __syncthreads();
         bin_keys();
@@ -1356,7 +1426,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
 // ------------------------------------------------------------- attention
 // Pages come from `sel` (global, logical ids, looked up through the page table), or, when
 // list_log is given, from lists in shared memory of (logical, physical) pages.
-template <int CL, int GM>
+template <int CL, int GM, bool SPLIT>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
                              const int32_t* sel, bool sel_coherent, bool q_staged, uint8_t* ring, SmallShared& sh,
                              const int32_t* list_log = nullptr, const int32_t* list_phys = nullptr) {
@@ -1618,7 +1688,7 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
                 }
             }
         }
-        if (S > 1) {
+        if (SPLIT && S > 1) {
             // this cluster's (m, l, o) of the head into the workspace; the last of the S
             // clusters to arrive (an atomic count, no waiting) merges them
             float* gp = a.attn_part + (qh_idx * kMaxSplits + z) * kPartStride;
@@ -1699,8 +1769,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
         cluster_sync_all();   // this CTA's shared data stays readable until every CTA is done with it
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
-        attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, false,
-                             false, big, sh);
+        attend_pages<CL, GM, true>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap,
+                                   false, false, big, sh);
     } else {
         bool listed = false;
         const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, true, &listed);
@@ -1711,8 +1781,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
         }
         // fast selection: every CTA holds the kept pages, ascending, in its gathered list
         const CandList kept = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
-        attend_pages<CL, GM>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap, true,
-                             true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr);
+        attend_pages<CL, GM, false>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap,
+                                    true, true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr);
     }
 }
 
