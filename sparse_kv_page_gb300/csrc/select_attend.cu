@@ -249,67 +249,12 @@ __device__ __forceinline__ float key_of_image(uint32_t u) {
 // over the partials of the scorer CTAs whose item range covers sequence b; no exchange.
 // Without partials: each CTA reduces its own pages' scores (staged rows or global
 // loads) and the CTAs exchange their (max, sum) through DSMEM.
+// The normaliser from this CTA's own scores and a cluster exchange (launches without the
+// scorer's partials): out of line, so that the partials path's code is contiguous.
 template <int CL, int GM>
-__device__ void normaliser(const SelectAttendArgs& a, int b, int kvh, int g, int j0, int j1, bool staged,
-                           const float* stg, int chunk, SmallShared& sh) {
+__device__ __noinline__ void normaliser_scores(const SelectAttendArgs& a, int b, int kvh, int g, int j0, int j1,
+                                             bool staged, const float* stg, int chunk, SmallShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (a.lse_partials) {
-        const int np = kStageUnits / a.hkv;
-        const int nchunks = (a.max_pages + np - 1) / np;
-        const int grid = max(1, a.score_grid);
-        const int per = max(1, (a.batch * nchunks + grid - 1) / grid);   // no items: c_hi < c_lo, n = 0
-        const int W = slot_warps(a.hkv, g);
-        const int c_lo = (b * nchunks) / per;
-        const int c_hi = min(grid - 1, ((b + 1) * nchunks - 1) / per);
-        const int n = (c_hi - c_lo + 1) * W;
-#pragma unroll 1
-        for (int hh = warp; hh < g; hh += kWarps) {
-            const float2* row = reinterpret_cast<const float2*>(a.lse_partials) +
-                                (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * grid * W + c_lo * W;
-            float m = -INFINITY, l = 0.f;
-            // two (max, sum) pairs per 16-byte load (a slot row starts on an even pair: W is even)
-#pragma unroll 1
-            for (int i0 = 0; i0 < n; i0 += 2 * 32 * 8) {
-                float4 v[8];   // all in flight before any use
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = i0 + 2 * (lane + 32 * u);
-                    v[u] = i < n ? __ldcg(reinterpret_cast<const float4*>(row + i))
-                                 : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-                }
-                // an empty or corrupt pair (sum not > 0, or a NaN) contributes nothing
-                float mm[16];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    mm[2 * u] = (v[u].y > 0.f && v[u].x == v[u].x) ? v[u].x : -INFINITY;
-                    mm[2 * u + 1] = (v[u].w > 0.f && v[u].z == v[u].z) ? v[u].z : -INFINITY;
-                }
-                float M = m;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) M = fmaxf(M, mm[k]);
-                if (M != -INFINITY) {
-                    float z = m == -INFINITY ? 0.f : l * fast_exp2((m - M) * kLog2e);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        z += mm[2 * u] == -INFINITY ? 0.f : v[u].y * fast_exp2((mm[2 * u] - M) * kLog2e);
-                        z += mm[2 * u + 1] == -INFINITY ? 0.f : v[u].w * fast_exp2((mm[2 * u + 1] - M) * kLog2e);
-                    }
-                    m = M;
-                    l = z;
-                }
-            }
-            float M = m;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float z = (m == -INFINITY) ? 0.f : l * fast_exp2((m - M) * kLog2e);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-            if (lane == 0) sh.Lh[hh] = (z > 0.f) ? M + logf(z) : -INFINITY;
-        }
-        __syncthreads();
-        return;
-    }
-
     // from this CTA's scores, then a cluster exchange
     const int64_t stride = a.max_pages;
     const float* srow = a.scores + (static_cast<int64_t>(b) * a.hq + kvh * g) * stride;
@@ -403,6 +348,69 @@ __device__ void normaliser(const SelectAttendArgs& a, int b, int kvh, int g, int
         sh.Lh[tid] = (z > 0.f) ? M + logf(z) : -INFINITY;
     }
     __syncthreads();
+}
+
+template <int CL, int GM>
+__device__ void normaliser(const SelectAttendArgs& a, int b, int kvh, int g, int j0, int j1, bool staged,
+                           const float* stg, int chunk, SmallShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (a.lse_partials) {
+        const int np = kStageUnits / a.hkv;
+        const int nchunks = (a.max_pages + np - 1) / np;
+        const int grid = max(1, a.score_grid);
+        const int per = max(1, (a.batch * nchunks + grid - 1) / grid);   // no items: c_hi < c_lo, n = 0
+        const int W = slot_warps(a.hkv, g);
+        const int c_lo = (b * nchunks) / per;
+        const int c_hi = min(grid - 1, ((b + 1) * nchunks - 1) / per);
+        const int n = (c_hi - c_lo + 1) * W;
+#pragma unroll 1
+        for (int hh = warp; hh < g; hh += kWarps) {
+            const float2* row = reinterpret_cast<const float2*>(a.lse_partials) +
+                                (static_cast<int64_t>(b) * a.hq + kvh * g + hh) * grid * W + c_lo * W;
+            float m = -INFINITY, l = 0.f;
+            // two (max, sum) pairs per 16-byte load (a slot row starts on an even pair: W is even)
+#pragma unroll 1
+            for (int i0 = 0; i0 < n; i0 += 2 * 32 * 8) {
+                float4 v[8];   // all in flight before any use
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + 2 * (lane + 32 * u);
+                    v[u] = i < n ? __ldcg(reinterpret_cast<const float4*>(row + i))
+                                 : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+                }
+                // an empty or corrupt pair (sum not > 0, or a NaN) contributes nothing
+                float mm[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    mm[2 * u] = (v[u].y > 0.f && v[u].x == v[u].x) ? v[u].x : -INFINITY;
+                    mm[2 * u + 1] = (v[u].w > 0.f && v[u].z == v[u].z) ? v[u].z : -INFINITY;
+                }
+                float M = m;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) M = fmaxf(M, mm[k]);
+                if (M != -INFINITY) {
+                    float z = m == -INFINITY ? 0.f : l * fast_exp2((m - M) * kLog2e);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        z += mm[2 * u] == -INFINITY ? 0.f : v[u].y * fast_exp2((mm[2 * u] - M) * kLog2e);
+                        z += mm[2 * u + 1] == -INFINITY ? 0.f : v[u].w * fast_exp2((mm[2 * u + 1] - M) * kLog2e);
+                    }
+                    m = M;
+                    l = z;
+                }
+            }
+            float M = m;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float z = (m == -INFINITY) ? 0.f : l * fast_exp2((m - M) * kLog2e);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            if (lane == 0) sh.Lh[hh] = (z > 0.f) ? M + logf(z) : -INFINITY;
+        }
+        __syncthreads();
+        return;
+    }
+    normaliser_scores<CL, GM>(a, b, kvh, g, j0, j1, staged, stg, chunk, sh);
 }
 
 // Bulk copy of rows [h0, h0 + nh) of this CTA's score columns [j0, j0 + nloc) to the
@@ -1132,12 +1140,13 @@ __device__ __noinline__ int select_general(const SelectAttendArgs& a, int b, int
 // ordered compaction (the pass counts place each CTA's kept keys in the output).
 template <int CL, int GM>
 __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int chunk, uint8_t* big,
-                            SmallShared& sh, bool stage_q, bool* listed) {
+                            SmallShared& sh, bool stage_q, bool* listed, bool* preissued) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* keys = reinterpret_cast<uint32_t*>(big);
     const CandList pub = cand_list(big + region_a_bytes(chunk, CL));
     const CandList cand = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
     *listed = false;
+    *preissued = false;
     const int g = a.hq / a.hkv;
     // This CTA's nominal page range [jn0, jn0 + nn). Inputs go out before the wait for the
     // scorer (an L2 prefetch of the range's page-table entries, the query rows, the
@@ -1419,6 +1428,30 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
             if (pos[u] >= s0 && pos[u] < s1) out[pos[u]] = cl[u];
         }
     }
+    // the first pages of every warp's attention share go out now: their K/V tiles into the
+    // ring (free: the keys and page-table rows it overlays are no longer read; the cluster
+    // barrier ordered every thread's reads before this fence), so the attention starts on
+    // tiles in flight. Launches with tail pages divide the attention differently: not those.
+    if (stage_q && paged && !a.tail_tokens) {
+        constexpr int kSlots = slots_per_warp(CL);
+        fence_proxy_async_smem();
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int q = pos[u] - s0;
+            if (kp[u] && pos[u] >= s0 && pos[u] < s1 && q < kSlots * kWarps) {
+                const int sl = q / kWarps * kWarps + q % kWarps;   // slot k = q / kWarps of warp q % kWarps
+                uint8_t* slot = big + sl * kPageSlotBytes;
+                uint64_t* bar = &sh.bar[sl];
+                const int y = static_cast<int>((static_cast<int64_t>(cp[u]) * a.hkv + kvh) * kPage);
+                mbar_arrive_expect_tx(bar, kPageSlotBytes);
+                tma_load_2d(slot, &a.tm_k, 0, y, bar);
+                tma_load_2d(slot + kBoxBytes, &a.tm_k, 64, y, bar);
+                tma_load_2d(slot + 2 * kBoxBytes, &a.tm_v, 0, y, bar);
+                tma_load_2d(slot + 3 * kBoxBytes, &a.tm_v, 64, y, bar);
+            }
+        }
+        *preissued = true;
+    }
     *listed = true;
     __syncthreads();
     return K;
@@ -1429,7 +1462,8 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
 template <int CL, int GM, bool SPLIT>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
                              const int32_t* sel, bool sel_coherent, bool q_staged, uint8_t* ring, SmallShared& sh,
-                             const int32_t* list_log = nullptr, const int32_t* list_phys = nullptr) {
+                             const int32_t* list_log = nullptr, const int32_t* list_phys = nullptr,
+                             bool preissued = false) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, t = lane & 3;
     const int g = a.hq / a.hkv;
@@ -1502,9 +1536,11 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             tma_load_2d(slot + 3 * kBoxBytes, &a.tm_v, 64, y, bar);
         }
     };
+    if (!preissued) {   // (the fused launch's selection issues a warp's first pages itself)
 #pragma unroll
-    for (int k = 0; k < kSlots; ++k)
-        if (p0 + warp + k * kWarps < p1) issue(p0 + warp + k * kWarps, k);
+        for (int k = 0; k < kSlots; ++k)
+            if (p0 + warp + k * kWarps < p1) issue(p0 + warp + k * kWarps, k);
+    }
     uint32_t phases = 0u;   // bit sl: the parity slot sl waits for next
     int sl = 0;
     for (int p = p0 + warp; p < p1; p += kWarps) {
@@ -1764,16 +1800,16 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     __syncthreads();
 
     if constexpr (MODE == SAMode::kSelect) {
-        bool listed = false;
-        select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, false, &listed);
+        bool listed = false, preissued = false;
+        select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, false, &listed, &preissued);
         cluster_sync_all();   // this CTA's shared data stays readable until every CTA is done with it
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
         attend_pages<CL, GM, true>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap,
                                    false, false, big, sh);
     } else {
-        bool listed = false;
-        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, true, &listed);
+        bool listed = false, preissued = false;
+        const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, true, &listed, &preissued);
         if (!listed) {
             // the selection went to global memory; make it visible to the cluster's CTAs
             asm volatile("fence.acq_rel.cluster;" ::: "memory");
@@ -1782,7 +1818,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
         // fast selection: every CTA holds the kept pages, ascending, in its gathered list
         const CandList kept = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
         attend_pages<CL, GM, false>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap,
-                                    true, true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr);
+                                    true, true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr,
+                                    preissued);
     }
 }
 
