@@ -1352,15 +1352,23 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
     }
     // the bin's keys, unordered, for the ranking
     auto bin_keys = [&]() {
+        // one shared atomic per warp for its three rounds
+        bool m[3];
+        unsigned bal[3];
 #pragma unroll
         for (int u = 0; u < 3; ++u) {
-            const bool m = cv[u] && static_cast<uint64_t>(ck[u]) < hi_u;
-            const unsigned bal = __ballot_sync(0xffffffffu, m);
-            int bpos = 0;
-            if (lane == 0 && bal) bpos = atomicAdd(&sh.nbin, __popc(bal));
-            bpos = __shfl_sync(0xffffffffu, bpos, 0);
-            const int at = bpos + __popc(bal & lanemask_lt());
-            if (m && at < kRankCap) sh.rank_keys[at] = ck[u];   // always: the bin count was checked
+            m[u] = cv[u] && static_cast<uint64_t>(ck[u]) < hi_u;
+            bal[u] = __ballot_sync(0xffffffffu, m[u]);
+        }
+        const int n0 = __popc(bal[0]), n1 = __popc(bal[1]), n2 = __popc(bal[2]);
+        int base = 0;
+        if (lane == 0 && n0 + n1 + n2 > 0) base = atomicAdd(&sh.nbin, n0 + n1 + n2);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const unsigned lt = lanemask_lt();
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int at = base + (u > 0 ? n0 : 0) + (u > 1 ? n1 : 0) + __popc(bal[u] & lt);
+            if (m[u] && at < kRankCap) sh.rank_keys[at] = ck[u];   // always: the bin count was checked
         }
     };
     bin_keys();
@@ -1380,17 +1388,31 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
         bin_keys();
         __syncthreads();
     }
+    // rank every bin key against all of them: G threads per key (consecutive lanes), each
+    // over a strided share, as many as the block holds (G a power of two <= 8)
     const int nb = min(sh.nbin, kRankCap);
-    if (tid < nb) {
-        const uint32_t key = sh.rank_keys[tid];
+    const int G = nb <= kThreads / 8 ? 8 : (nb <= kThreads / 4 ? 4 : (nb <= kThreads / 2 ? 2 : 1));
+    {
+        const int kidx = tid / G, part = tid % G;
+        const uint32_t key = kidx < nb ? sh.rank_keys[kidx] : 0u;
         int gt = 0, ge = 0;
-#pragma unroll 8
-        for (int q = 0; q < nb; ++q) {
-            const uint32_t v = sh.rank_keys[q];
-            gt += v > key;
-            ge += v >= key;
+        if (kidx < nb) {
+#pragma unroll 4
+            for (int q = part; q < nb; q += G) {
+                const uint32_t v = sh.rank_keys[q];
+                gt += v > key;
+                ge += v >= key;
+            }
         }
-        if (gt < remaining && ge >= remaining) {   // key is the remaining-th largest of the bin
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {   // sum over the key's G lanes (aligned groups)
+            const int gt2 = __shfl_xor_sync(0xffffffffu, gt, o), ge2 = __shfl_xor_sync(0xffffffffu, ge, o);
+            if (o < G) {
+                gt += gt2;
+                ge += ge2;
+            }
+        }
+        if (kidx < nb && part == 0 && gt < remaining && ge >= remaining) {   // the remaining-th largest
             sh.rank_T = key;
             sh.rank_take = remaining - gt;
             sh.rank_eq = ge - gt;
