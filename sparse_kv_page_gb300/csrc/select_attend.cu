@@ -76,10 +76,19 @@ __host__ __device__ constexpr int ring_bytes(int cl) {
 // Shared memory after SmallShared: region A (the keys, which overlay the staged score rows
 // of four heads, then the attention ring), then (selection) the published and the gathered
 // candidate lists.
+// 12-CTA clusters merge the attention by pushing each CTA's per-head partial into the
+// owning CTA's inbox (after every other region): slot (head / CL, source CTA), each
+// [m, l, 2 pad, o[128]] floats; a CTA owns at most two of up to 16 heads.
+constexpr int kInStride = 4 + kD;
+constexpr int kInboxBytes = 2 * kSpreadCluster * kInStride * 4;
 __host__ __device__ constexpr int region_a_bytes(int chunk, int cl) {
     return (4 * chunk * 4 <= stage_cap(cl) && round_kib(4 * chunk * 4) > ring_bytes(cl)) ? round_kib(4 * chunk * 4)
            : round_kib(chunk * 4) > ring_bytes(cl)                                        ? round_kib(chunk * 4)
                                                                                            : ring_bytes(cl);
+}
+// byte offset of the inbox from the region after SmallShared
+__host__ __device__ constexpr int inbox_offset(int chunk, int cl, bool attend_only) {
+    return attend_only ? ring_bytes(cl) : region_a_bytes(chunk, cl) + 2 * kCandListBytes;
 }
 
 struct SmallShared {
@@ -120,6 +129,15 @@ __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float 
     if (M == -INFINITY) return;
     l = l * fast_exp2((m - M) * kLog2e) + l2 * fast_exp2((m2 - M) * kLog2e);
     m = M;
+}
+
+// Stores into another CTA's shared memory (cluster-window addresses from dsmem_addr).
+__device__ __forceinline__ void st_dsmem_f32x2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f32x4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
 // ------------------------------------------------------------- selection
@@ -1484,7 +1502,7 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
 template <int CL, int GM, bool SPLIT>
 __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t rank, int n_sel,
                              const int32_t* sel, bool sel_coherent, bool q_staged, uint8_t* ring, SmallShared& sh,
-                             const int32_t* list_log = nullptr, const int32_t* list_phys = nullptr,
+                             float* inbox, const int32_t* list_log = nullptr, const int32_t* list_phys = nullptr,
                              bool preissued = false) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gid = lane >> 2, t = lane & 3;
@@ -1710,29 +1728,47 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
                 acc3 += r[5 + d4] * f;
             }
         }
-        float* c = sh.cpart + hh * kPartStride;
-        if (d4 == 0) {
-            c[0] = M;
-            c[1] = L;
+        if constexpr (CL == kSpreadCluster) {
+            // into the owner's inbox: slot (hh / CL, this CTA)
+            const uint32_t ra = dsmem_addr(inbox + ((hh / CL) * CL + static_cast<int>(rank)) * kInStride,
+                                           static_cast<uint32_t>(hh % CL));
+            if (d4 == 0) st_dsmem_f32x2(ra, M, L);
+            st_dsmem_f32x4(ra + static_cast<uint32_t>(4 + d4) * 4u, acc0, acc1, acc2, acc3);
+        } else {
+            float* c = sh.cpart + hh * kPartStride;
+            if (d4 == 0) {
+                c[0] = M;
+                c[1] = L;
+            }
+            c[2 + d4] = acc0;
+            c[3 + d4] = acc1;
+            c[4 + d4] = acc2;
+            c[5 + d4] = acc3;
         }
-        c[2 + d4] = acc0;
-        c[3 + d4] = acc1;
-        c[4 + d4] = acc2;
-        c[5 + d4] = acc3;
     }
-    cluster_sync_all();
+    cluster_sync_all();   // every CTA's partials delivered (pushed) or readable (pulled)
     // cluster merge: CTA r finalises heads r, r + CL, ...
     for (int hh = static_cast<int>(rank); hh < g; hh += CL) {
         const int64_t qh_idx = static_cast<int64_t>(b) * a.hq + kvh * g + hh;
         float M = -INFINITY, L = 0.f, acc = 0.f;
         if (tid < kD) {
-            const float* c = sh.cpart + hh * kPartStride;
-            float mr[CL], lr[CL], orr[CL];   // all remote loads in flight before any use
+            float mr[CL], lr[CL], orr[CL];   // all loads in flight before any use
+            if constexpr (CL == kSpreadCluster) {
+                const float* in = inbox + (hh / CL) * CL * kInStride;
 #pragma unroll
-            for (uint32_t r = 0; r < CL; ++r) {
-                mr[r] = ld_dsmem_f32(dsmem_addr(c, r));
-                lr[r] = ld_dsmem_f32(dsmem_addr(c + 1, r));
-                orr[r] = ld_dsmem_f32(dsmem_addr(c + 2 + tid, r));
+                for (int r = 0; r < CL; ++r) {
+                    mr[r] = in[r * kInStride];
+                    lr[r] = in[r * kInStride + 1];
+                    orr[r] = in[r * kInStride + 4 + tid];
+                }
+            } else {
+                const float* c = sh.cpart + hh * kPartStride;
+#pragma unroll
+                for (uint32_t r = 0; r < CL; ++r) {
+                    mr[r] = ld_dsmem_f32(dsmem_addr(c, r));
+                    lr[r] = ld_dsmem_f32(dsmem_addr(c + 1, r));
+                    orr[r] = ld_dsmem_f32(dsmem_addr(c + 2 + tid, r));
+                }
             }
 #pragma unroll
             for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, mr[r]);
@@ -1786,7 +1822,8 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
             if (a.lse && tid == 0) a.lse[qh_idx] = (L > 0.f) ? (M + fast_log2(L)) * kLn2 : -INFINITY;
         }
     }
-    cluster_sync_all();   // partials stay readable until every CTA is done
+    // pulled partials stay readable until every CTA is done; pushed ones are local
+    if constexpr (CL != kSpreadCluster) cluster_sync_all();
 }
 
 template <int CL, SAMode MODE, int GM>
@@ -1828,7 +1865,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
     } else if constexpr (MODE == SAMode::kAttend) {
         const int n = max(0, min(a.n_selected[b * a.hkv + kvh], a.k_cap));
         attend_pages<CL, GM, true>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap,
-                                   false, false, big, sh);
+                                   false, false, big, sh, reinterpret_cast<float*>(big + inbox_offset(chunk, CL, true)));
     } else {
         bool listed = false, preissued = false;
         const int n = select_pages<CL, GM>(a, b, kvh, rank, chunk, big, sh, true, &listed, &preissued);
@@ -1840,8 +1877,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid
         // fast selection: every CTA holds the kept pages, ascending, in its gathered list
         const CandList kept = cand_list(big + region_a_bytes(chunk, CL) + kCandListBytes);
         attend_pages<CL, GM, false>(a, b, kvh, rank, n, a.selected + (static_cast<int64_t>(b) * a.hkv + kvh) * a.k_cap,
-                                    true, true, big, sh, listed ? kept.logical : nullptr, listed ? kept.phys : nullptr,
-                                    preissued);
+                                    true, true, big, sh, reinterpret_cast<float*>(big + inbox_offset(chunk, CL, false)),
+                                    listed ? kept.logical : nullptr, listed ? kept.phys : nullptr, preissued);
     }
 }
 
@@ -1968,7 +2005,7 @@ size_t select_attend_smem_bytes(int max_pages, int cluster, SAMode mode) {
         mode == SAMode::kAttend
             ? small + static_cast<size_t>(ring_bytes(cluster))
             : small + static_cast<size_t>(region_a_bytes(chunk_of(max_pages, cluster), cluster)) + 2 * kCandListBytes;
-    return cluster == kSpreadCluster ? std::max<size_t>(need, kSpreadSmemBytes) : need;
+    return cluster == kSpreadCluster ? std::max<size_t>(need + kInboxBytes, kSpreadSmemBytes) : need;
 }
 
 int group_bound(int g) { return g <= 4 ? 4 : 16; }
