@@ -365,10 +365,31 @@ def test_selection_parity_every_cluster_size(pin_cluster, cluster, g, hkv, budge
 
 
 @pytest.mark.parametrize("cluster", [8, 12, 16])
-@pytest.mark.parametrize("wname,pages,batch,budget", [("ctx1m", 900, 1, 2048), ("glm9b_4x1m", 600, 2, 512)])
+@pytest.mark.parametrize("wname,pages,batch,budget", [("ctx1m", 900, 1, 2048), ("glm9b_4x1m", 600, 2, 512),
+                                                      ("ctx1m", 2400, 1, 8192)])
 def test_decode_step_every_cluster_size(pin_cluster, cluster, wname, pages, batch, budget):
+    """The fused step at each cluster size; budget 8192 keeps 512 pages per (sequence, kv
+    head), more than a CTA's warps take in their first ring slots, so the attention refills
+    slots behind the tiles the selection issued."""
     pin_cluster(cluster)
     _check_decode_step(wname, pages, batch, budget)
+
+
+@pytest.mark.parametrize("cluster", [8, 12, 16])
+def test_selection_candidates_concentrated_in_one_cta(pin_cluster, cluster):
+    """The K largest keys all lie in the first CTA's page range, so that CTA publishes more
+    candidates than its fixed gather slots (kCandCap / cluster) and every CTA regathers
+    by offsets; the selection is still the oracle's."""
+    pin_cluster(cluster)
+    rng = np.random.default_rng(11 + cluster)
+    B, hkv, g, maxp = 1, 2, 4, 3000
+    scores = rng.standard_normal((B, hkv * g, maxp)) * 0.3
+    scores[:, :, :200] += 6.0    # the first 200 pages (inside CTA 0's range at any cluster size) dominate
+    seq = np.array([maxp], np.int32)
+    budget = 150 * 16
+    sel, n, keys, osel, on, okeys = _select_case(scores, seq, budget, hkv)
+    check_selection(sel, n, osel, on, okeys, seq)
+    assert np.all(sel[0, :, :150] < 200)
 
 
 def _check_decode_step(wname, pages, batch, budget):
