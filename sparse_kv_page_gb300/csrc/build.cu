@@ -13,7 +13,7 @@
 //   quantisation to int8 / int4 / int8 with fp16 scales, packed in the
 //   scorer's fragment order (see include/locks.h).
 //
-// GPU mapping: a warp builds two units at a time (three CTAs of four warps per SM; the
+// GPU mapping: a warp builds two units at a time (four CTAs of four warps per SM; the
 // keys stay in bf16 in shared memory and the deviations are formed on the fly). The Gram
 // matrix runs on the tensor cores (f16 hi/lo split of the power-of-two-normalised deviations,
 // three MMAs per tile, fp32 accumulate); the Jacobi sweeps keep one row of G
@@ -31,10 +31,10 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kKStride = 136;   // bf16 row stride of the keys in shared memory (conflict-free fragments)
 constexpr int kMaxSweeps = 10;
 constexpr int64_t kSingleUnitBuild = 512;   // builds of at most this many units: one unit per warp
-constexpr int kCtasPerSm = 3;   // 12 warps per SM at 168 registers (the shared memory allows it)
+constexpr int kCtasPerSm = 4;   // 16 warps per SM: 128 registers (no spills), 4 x 56 KB of shared memory
 
 // The keys stay in bf16 (exact) and D = K - mu is formed on the fly in fp32, which keeps
-// the per-warp footprint small enough for three CTAs per SM.
+// the per-warp footprint small enough for four CTAs per SM.
 struct WarpSmem {
     uint16_t k[2][kPage * kKStride];
     float mu[2][kD];
