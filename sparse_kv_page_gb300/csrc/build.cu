@@ -171,7 +171,7 @@ __device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, 
     __syncwarp();
     // mean over the 16 keys, lane -> dims 4 lane .. 4 lane + 3
     float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 4
     for (int i = 0; i < kPage; ++i) {
         const uint2 v = *reinterpret_cast<const uint2*>(k + i * kKStride + 4 * lane);
         s4[0] += bf16_lo(v.x);
@@ -183,7 +183,7 @@ __device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, 
     for (int q = 0; q < 4; ++q) s4[q] *= (1.f / kPage);
     *reinterpret_cast<float4*>(mu + 4 * lane) = make_float4(s4[0], s4[1], s4[2], s4[3]);
     float amax = 0.f;
-#pragma unroll
+#pragma unroll 4
     for (int i = 0; i < kPage; ++i) {
         const uint2 v = *reinterpret_cast<const uint2*>(k + i * kKStride + 4 * lane);
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x) - s4[0]), fabsf(bf16_hi(v.x) - s4[1])),
@@ -198,7 +198,9 @@ __device__ void load_centre_gram(const BuildArgs& a, int64_t unit, WarpSmem& w, 
     e = max(-100, min(100, e));
     const float inv = __int_as_float((127 - e) << 23);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
+    // once-per-unit loops stay rolled: the code of all phases of the 16 warps of an SM
+    // shares the instruction caches with the Jacobi round loop
+#pragma unroll 2
     for (int s = 0; s < 8; ++s) {
         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -312,7 +314,7 @@ __device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int s
     for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int r = 0; r < kRank; ++r) v[q][r] = 0.f;
-#pragma unroll
+#pragma unroll 2
     for (int i = 0; i < kPage; ++i) {
         const uint2 kv = *reinterpret_cast<const uint2*>(k + i * kKStride + 4 * lane);
         const float4 ua = *reinterpret_cast<const float4*>(u8 + i * kRank);
