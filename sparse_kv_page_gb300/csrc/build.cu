@@ -278,14 +278,14 @@ __device__ void jacobi_top8(WarpSmem& w, int lane) {
     // rank of this eigenvalue (descending, ties -> lower index)
     int rk = 0;
     float lam1 = lam;
-#pragma unroll
+#pragma unroll 4
     for (int j = 0; j < 16; ++j) {
         const float lj = __shfl_sync(0xffffffffu, lam, base + j);
         rk += (lj > lam) || (lj == lam && j < i);
         lam1 = fmaxf(lam1, lj);
     }
     const float scale = __int_as_float((127 + e) << 23);   // 2^e: undo the Gram normalisation
-#pragma unroll
+#pragma unroll 1
     for (int r = 0; r < kRank; ++r) {
         // column index (lane within the half) holding rank r
         const unsigned bal = __ballot_sync(0xffffffffu, rk == r);
@@ -402,7 +402,7 @@ __device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int s
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
         uint32_t word = 0;
-#pragma unroll
+#pragma unroll 1
         for (int bi = 0; bi < 4; ++bi) {
             const int ob = 16 * lane + 4 * wi + bi;
             const int r = ob >> 6, rem = ob & 63, t = rem >> 4, j = (rem & 15) >> 2, pb = rem & 3;
@@ -419,7 +419,7 @@ __device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int s
     // mu byte o: t = o / 32, s = (o % 32) / 4, h = (o % 4) / 2, e = o % 2
     {
         uint32_t word = 0;
-#pragma unroll
+#pragma unroll 1
         for (int bi = 0; bi < 4; ++bi) {
             const int o = 4 * lane + bi;
             const int t = o >> 5, s = (o & 31) >> 2, h = (o & 3) >> 1, e = o & 1;
@@ -432,7 +432,7 @@ __device__ void finish_unit(const BuildArgs& a, int64_t unit, WarpSmem& w, int s
     // coef byte o: lane' = o / 4 (gid' = lane' / 4, t' = lane' % 4), i = gid' + 8 ((o % 4) / 2), r = 2 t' + o % 2
     {
         uint32_t word = 0;
-#pragma unroll
+#pragma unroll 1
         for (int bi = 0; bi < 4; ++bi) {
             const int o = 4 * lane + bi;
             const int lp = o >> 2, gp = lp >> 2, tp = lp & 3;
