@@ -1827,7 +1827,7 @@ __device__ void attend_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t
 }
 
 template <int CL, SAMode MODE, int GM>
-__global__ void __launch_bounds__(kThreads, 2) select_attend_kernel(const __grid_constant__ SelectAttendArgs a,
+__global__ void __launch_bounds__(kThreads, CL == kSpreadCluster ? 1 : 2) select_attend_kernel(const __grid_constant__ SelectAttendArgs a,
                                                                        int chunk) {
     extern __shared__ __align__(1024) uint8_t smem[];
     SmallShared& sh = *reinterpret_cast<SmallShared*>(smem);
