@@ -12,20 +12,26 @@
 // selection"; LOCKS post, "Code": keep budget // 16 pages, sorted ascending):
 //   L_h   = log sum_j exp(s_hj)                      (per query head)
 //   key_j = log((1/g) sum_{h in group} exp(s_hj - L_h))
-//   top-k by an MSB-first radix select (4 passes of 8 bits) on the
-//   order-preserving uint32 image of key_j; histograms are summed across the
-//   cluster through DSMEM. Equal keys are ranked by lower page id; the output
-//   is written in ascending page order by an ordered compaction.
+//   top-k by a radix select on the order-preserving uint32 image of key_j:
+//   a first 8-bit pass over the range the keys' sum fixes, built with the
+//   keys; its histograms summed across the cluster through DSMEM; then the
+//   candidates (keys in and above the chosen bin) gathered into every CTA and
+//   the bin ranked directly (an exact MSB-first radix out of line when that
+//   fails). Equal keys are ranked by lower page id; the kept pages are written
+//   in ascending page order.
 // Attention (LOCKS post, "Code": scaled dot-product attention over the pages
 // kept): each CTA takes a contiguous share of the selected pages; each warp
-// streams one page at a time (its K and V rows as four tiled TMA boxes of 16
-// tokens x 64 dims, 128-byte swizzle) and runs QK^T and PV on the tensor cores
-// (mma.sync bf16 through ldmatrix, query split hi/lo, online softmax in fp32).
-// Warp partials (m, l, o) are merged per CTA, then across the cluster.
+// streams its pages (K and V rows as four tiled TMA boxes of 16 tokens x 64
+// dims, 128-byte swizzle; one or two ring slots per warp) and runs QK^T and PV
+// on the tensor cores (mma.sync bf16 through ldmatrix, query split hi/lo,
+// online softmax in fp32). Warp partials (m, l, o) are merged per CTA, then
+// across the cluster (pulled through DSMEM, or, on 12-CTA clusters, pushed
+// into the owning CTA).
 //
 // When the scoring kernel's per-8-page LSE partials are given, the per-head
 // normaliser L_h is reduced from them instead of from the full score table.
-// At most 128 registers per thread so that two CTAs share an SM.
+// 8- and 16-CTA instances keep to 128 registers per thread so that two CTAs
+// share an SM; 12-CTA instances run one CTA per SM.
 #include <cudaTypedefs.h>
 #include <algorithm>
 #include <climits>
