@@ -138,6 +138,9 @@ __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float 
 }
 
 // Stores into another CTA's shared memory (cluster-window addresses from dsmem_addr).
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_dsmem_f32x2(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
@@ -948,10 +951,15 @@ __device__ __noinline__ int publish_ordered_ool(const SelectAttendArgs& a, int b
 // CTAs, this CTA), eq_low / eq_own / inbin (keys in the bin: lower-ranked, own, all).
 template <int CL>
 __device__ __forceinline__ void pick_digit(const uint32_t* hist, int remaining, uint32_t rank, SmallShared& sh,
-                                           uint32_t (&hv)[CL]) {
+                                           uint32_t (&hv)[CL], const uint32_t* pushed = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (pushed) {   // every CTA's histogram already pushed here: [rank][bin]
 #pragma unroll
-    for (uint32_t r = 0; r < CL; ++r) hv[r] = ld_dsmem_u32(dsmem_addr(&hist[tid], r));   // all in flight
+        for (uint32_t r = 0; r < CL; ++r) hv[r] = pushed[r * 256 + tid];
+    } else {
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) hv[r] = ld_dsmem_u32(dsmem_addr(&hist[tid], r));   // all in flight
+    }
     uint32_t all = 0u, low = 0u;
 #pragma unroll
     for (uint32_t r = 0; r < CL; ++r) {
@@ -1235,10 +1243,20 @@ __device__ int select_pages(const SelectAttendArgs& a, int b, int kvh, uint32_t 
         return K;
     }
 
-    // pass 0 over the fast range (its histogram was built with the keys)
+    // pass 0 over the fast range (its histogram was built with the keys). 12-CTA clusters
+    // push each bin to every CTA before the barrier (a table in the merge inbox, which is
+    // unused until the attention), so the digit is picked from local memory.
+    uint32_t* pushed = nullptr;
+    if constexpr (CL == kSpreadCluster) {
+        pushed = reinterpret_cast<uint32_t*>(big + inbox_offset(chunk, CL, false));
+        static_assert(CL * 256 * 4 <= kInboxBytes, "the histogram table fits the inbox");
+        const uint32_t mine = sh.hist[0][tid];   // written by this thread (bin 0: thread 0)
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) st_dsmem_u32(dsmem_addr(&pushed[rank * 256 + tid], r), mine);
+    }
     cluster_sync_all();
     uint32_t hv[CL];
-    pick_digit<CL>(sh.hist[0], K, rank, sh, hv);
+    pick_digit<CL>(sh.hist[0], K, rank, sh, hv, pushed);
     const uint32_t digit = static_cast<uint32_t>(sh.digit);
     if (tid == static_cast<int>(digit)) {
 #pragma unroll
