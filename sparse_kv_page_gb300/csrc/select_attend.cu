@@ -28,8 +28,9 @@
 // across the cluster (pulled through DSMEM, or, on 12-CTA clusters, pushed
 // into the owning CTA).
 //
-// When the scoring kernel's per-8-page LSE partials are given, the per-head
-// normaliser L_h is reduced from them instead of from the full score table.
+// When the scoring kernel's LSE partials (one (max, sum exp) pair per scorer warp
+// and query head) are given, the per-head normaliser L_h is reduced from them
+// instead of from the full score table.
 // 8- and 16-CTA instances keep to 128 registers per thread so that two CTAs
 // share an SM; 12-CTA instances run one CTA per SM.
 #include <cudaTypedefs.h>
@@ -1908,7 +1909,7 @@ __global__ void __launch_bounds__(kThreads, CL == kSpreadCluster ? 1 : 2) select
 
 int chunk_of(int max_pages, int cluster) {
     int c = (max_pages + cluster - 1) / cluster;
-    return (c + 7) & ~7;   // whole 8-page blocks (the LSE partials' granularity)
+    return (c + 7) & ~7;   // whole 8-page blocks: 4-page slabs and 16-byte score loads stay aligned
 }
 
 // The driver's tiled tensor-map encoder, looked up once through the runtime.
